@@ -1,0 +1,180 @@
+/*
+ * pa.h — C ABI of the paged-KV attention library (GB300, sm_103a).
+ *
+ * The library implements the data-parallel hot path of a paged KV cache as the
+ * nano-vllm pages describe it:
+ *   - store:   each new token's K/V rows are scattered into k_cache/v_cache at the
+ *              row index slot_mapping[i] ("nano-vllm解读", section "KVCache的写入";
+ *              "3.6 ModelRunner、CUDA Graph 与性能基准", section 2, prepare_prefill /
+ *              prepare_decode, where slot = block_table[pos / block_size] * block_size
+ *              + pos % block_size and slot == -1 marks a padding row that is skipped).
+ *   - decode:  one query token per sequence attends over the first context_lens[b]
+ *              cached tokens, gathered through the -1-padded int32 block table
+ *              ("nano-vllm解读", sections "PageAttention原理" and "Nano-vllm中的使用").
+ *   - prefill: causal varlen attention of the new tokens of each sequence over its
+ *              cached prefix plus the new tokens, the key/value rows read through the
+ *              block table ("nano-vllm解读", section "如何适配不同请求不同序列长度";
+ *              "3.6 ModelRunner…", section 2, cu_seqlens_q / cu_seqlens_k).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer named as device memory is caller-owned CUDA device memory on the
+ *     current device. The library allocates nothing and frees nothing.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL =
+ *     the legacy default stream) and never synchronises the host.
+ *   - Element type: bf16 (raw 16-bit storage) for q, k, v, caches and outputs.
+ *     head_dim must be 128; anything else returns PA_ERR_UNSUPPORTED.
+ *   - Layouts are C-contiguous unless a stride argument says otherwise:
+ *       k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim]
+ *       block_tables      [num_seqs, max_blocks_per_seq] int32, right-padded with -1
+ *   - GQA: query head h reads KV head h / (num_heads / num_kv_heads).
+ *   - Host-side validation happens before any launch; when it fails the call returns
+ *     the status and launches nothing.
+ *   - Data-dependent errors that only the device can see (a block id outside
+ *     [0, num_blocks), a slot outside [-1, num_blocks*block_size), a context longer
+ *     than max_blocks_per_seq*block_size, a pipeline wait that ran out) never fault:
+ *     the offending access is skipped and, when `dev_err` is non-NULL, the matching
+ *     PA_DEV_ERR_* bit is OR-ed into *dev_err (device memory, one int). The host reads
+ *     it after synchronising. The output rows touched by such an error are undefined.
+ */
+#ifndef PAGED_KV_PA_H
+#define PAGED_KV_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side status codes returned by every entry point. */
+enum pa_status {
+  PA_OK = 0,
+  PA_ERR_NULL = 1,        /* a required pointer is NULL */
+  PA_ERR_SHAPE = 2,       /* inconsistent sizes: H % Hk != 0, block_size <= 0, ... */
+  PA_ERR_UNSUPPORTED = 3, /* head_dim != 128, or a size beyond what the kernels take */
+  PA_ERR_WORKSPACE = 4,   /* decode workspace missing or too small */
+  PA_ERR_CUDA = 5,        /* a CUDA runtime error (launch, attribute, tensor map) */
+  PA_ERR_ALIGN = 6        /* a pointer or stride breaks the 16-byte alignment rule */
+};
+
+/* Bits OR-ed into *dev_err by the kernels. */
+enum pa_dev_error {
+  PA_DEV_ERR_BLOCK_ID = 1, /* block table entry outside [0, num_blocks) where a read needs it */
+  PA_DEV_ERR_SLOT = 2,     /* slot_mapping entry outside [-1, num_blocks*block_size) */
+  PA_DEV_ERR_CONTEXT = 4,  /* context length above max_blocks_per_seq*block_size, or negative */
+  PA_DEV_ERR_TIMEOUT = 8,  /* a bounded pipeline wait gave up (the kernel returned early) */
+  PA_DEV_ERR_SEQLENS = 16  /* cu_seqlens not non-decreasing, or a sequence shape out of range */
+};
+
+/* Human-readable name of a pa_status value. Never NULL. */
+const char* pa_status_str(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+int pa_version(void);
+
+/*
+ * pa_store_kvcache — scatter new K/V rows into the paged cache.
+ * Source: "nano-vllm解读", section "KVCache的写入" (one Triton kernel writes each
+ * token's K/V at its slot); "3.6 ModelRunner…", section 2 (slot formula; slot == -1
+ * is a padding row that writes nothing).
+ *
+ *   k, v            device, bf16, token i's row starts at k + i*k_tok_stride elements
+ *                   and holds num_kv_heads*head_dim contiguous elements.
+ *   k_tok_stride,
+ *   v_tok_stride    token strides in ELEMENTS (>= num_kv_heads*head_dim).
+ *   k_cache,v_cache device, bf16 [num_blocks, block_size, num_kv_heads, head_dim],
+ *                   updated in place: row s of the [num_blocks*block_size,
+ *                   num_kv_heads*head_dim] view receives token i when slot_mapping[i]==s.
+ *   slot_mapping    device, int32 [num_tokens]; -1 = skip this token.
+ *   num_tokens      >= 0 (0 launches nothing and returns PA_OK).
+ *
+ * The copy is bit-exact. Two tokens with the same slot race (the pages never produce
+ * that). A 16-byte vector path is used when k, v, both caches and both strides are
+ * 16-byte aligned; otherwise a 2-byte path gives the same bytes.
+ */
+int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t v_tok_stride,
+                     void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
+                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                     int* dev_err, void* stream);
+
+/*
+ * pa_decode_workspace_size — bytes of scratch that pa_decode needs for num_seqs
+ * sequences and num_heads query heads on the CURRENT device (the size depends on its
+ * SM count). Returns 0 for invalid sizes.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim);
+
+/*
+ * pa_decode — paged GQA decode attention, one query token per sequence.
+ * Source: "nano-vllm解读", sections "PageAttention原理" (address = base +
+ * block_table[pos / block_size] * block_size + pos % block_size) and
+ * "Nano-vllm中的使用" (q [B, H, d]; caches [max_blocks, block_size, H_kv, d];
+ * cache_seqlens int32 [B]; block_table int32 [B, max_len_blocks] padded with -1;
+ * softmax_scale = 1/sqrt(head_dim)); "3.6 ModelRunner…", section 2 (context_lens =
+ * len(seq), i.e. the just-stored token is part of the context).
+ *
+ *   out             device, bf16 [num_seqs, num_heads, head_dim]; written for every row.
+ *   q               device, bf16 [num_seqs, num_heads, head_dim].
+ *   block_tables    device, int32 [num_seqs, max_blocks_per_seq]; entries at index
+ *                   >= ceil(context_lens[b]/block_size) are never read.
+ *   context_lens    device, int32 [num_seqs]; 0 writes a zero row and reads nothing.
+ *   scale           softmax scale; <= 0 or NaN means 1/sqrt(head_dim).
+ *   grid_ctas       number of CTAs that split the key stream (0 = one per SM). The result
+ *                   does not depend on it beyond fp32 rounding of the final combine.
+ *   workspace       device scratch of at least pa_decode_workspace_size(...) bytes,
+ *                   256-byte aligned. Its first num_seqs*num_kv_heads int32 words are
+ *                   arrival counters that must be ZERO before the first call; every
+ *                   successful call leaves them zero again (after a PA_DEV_ERR_TIMEOUT
+ *                   the caller must zero them). Calls that overlap in time must use
+ *                   different workspaces.
+ *
+ * Arithmetic: bf16 inputs, fp32 products, fp32 online softmax and accumulation, one
+ * bf16 round-to-nearest-even at the end.
+ */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+              size_t workspace_bytes, int* dev_err, void* stream);
+
+/*
+ * pa_prefill_varlen — causal (or full) varlen attention of new tokens over the paged
+ * cache, on the tcgen05 tensor cores.
+ * Source: "nano-vllm解读", section "如何适配不同请求不同序列长度" (q [sum_seq_lens, H, d];
+ * cu_seqlens_q / cu_seqlens_k cumulative lengths; max_seqlen_q / max_seqlen_k;
+ * causal=True; block_table given when a prefix is cached); "3.6 ModelRunner…",
+ * section 2 (new token i of sequence s sits at absolute position
+ * num_cached_tokens + i; cu_seqlens_k counts cached plus new tokens).
+ *
+ *   out             device, bf16 [cu_seqlens_q[num_seqs], num_heads, head_dim].
+ *   q               device, bf16, same shape as out.
+ *   k_cache,v_cache device, bf16 caches that ALREADY hold every key/value row of the
+ *                   call, the new tokens included (run pa_store_kvcache first).
+ *   block_tables    device, int32 [num_seqs, max_blocks_per_seq].
+ *   cu_seqlens_q    device, int32 [num_seqs+1]; n_s = cu_seqlens_q[s+1]-cu_seqlens_q[s].
+ *   cu_seqlens_k    device, int32 [num_seqs+1]; k_s = cu_seqlens_k[s+1]-cu_seqlens_k[s]
+ *                   = cached + new tokens, so the cached count is c_s = k_s - n_s >= 0.
+ *   max_seqlen_q    host bound on n_s (sizes the grid); sequences above it set
+ *                   PA_DEV_ERR_SEQLENS and are left unwritten.
+ *   max_seqlen_k    host bound on k_s, used for validation only.
+ *   causal          non-zero: query i of sequence s (absolute position c_s + i) sees keys
+ *                   t <= c_s + i. Zero: it sees all k_s keys.
+ *   scale           softmax scale; <= 0 or NaN means 1/sqrt(head_dim).
+ *
+ * Requirements: block_size a multiple of 128, or a divisor of 128 that is a multiple of
+ * 8; q, out and both caches 16-byte aligned. Arithmetic: bf16 tensor-core products
+ * with fp32 accumulation, fp32 softmax, P rounded to bf16 for the second product, one
+ * bf16 rounding of the output.
+ */
+int pa_prefill_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                      int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, int causal, float scale,
+                      int* dev_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_PA_H */
