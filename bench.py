@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode step on GB300.
+
+One step = one pass of the hot path over one batch: the store of every sequence's new
+token into the paged cache, then paged GQA decode attention over context_lens that
+include it (split across CTAs, partials combined in-kernel). The default workload is the
+Qwen3-0.6B-shaped decode step: B=256, context U{100..2048}, H=16, H_kv=8, D=128,
+block_size=256, a 4096-block pool, bf16.
+
+Metric: effective KV-read GB/s of the step (sum over sequences of context*H_kv*D*2*2
+bytes, divided by the step time), with seqs/s beside it. Inputs are larger than L2
+(about 1.1 GB of K/V per step), so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torch.distributed.run: every rank runs its own replica of the
+workload (weak scaling); there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: effective KV-read GB/s (% of GB300 HBM peak), seqs/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_traffic(kernel_src: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (sha256 recorded in the summary); otherwise None."""
+    path = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "paged_kv_cache_107_gb300", "csrc", kernel_src)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+        if m_sha and m_b and m_sha.group(1) == sha:
+            return float(m_b.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out_path = None
+
+    def __enter__(self):
+        try:
+            self.out_path = f"/tmp/pa_clocks_{os.getpid()}.csv"
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.out_path or not os.path.exists(self.out_path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out_path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.out_path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    if n_gpus <= 1 and "WORLD_SIZE" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_summary(case):
+    tot_ctx = case.total_context()
+    kv_bytes = tot_ctx * case.num_kv_heads * case.head_dim * 2 * 2
+    qo_bytes = case.num_seqs * case.num_heads * case.head_dim * 2 * 2
+    meta_bytes = case.block_tables.nbytes + case.context_lens.nbytes
+    store_bytes = int((case.slot_mapping >= 0).sum()) * case.num_kv_heads * case.head_dim * 2 * 2 * 2
+    return tot_ctx, kv_bytes, qo_bytes + meta_bytes, store_bytes
+
+
+def oracle_store(case):
+    import oracle
+    t0 = time.perf_counter()
+    ok, ov = oracle.store_kvcache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                  case.slot_mapping)
+    return ok, ov, time.perf_counter() - t0
+
+
+def cpu_baseline(case, seconds: float = 10.0, threads: int = 0, stored=None):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the workload: whole
+    sequences, all heads, until about `seconds` of CPU time has passed."""
+    import numpy as np
+    import oracle
+    cores = oracle.max_threads(threads)
+    # the store of the step (once), then decode over consecutive sequences of the batch
+    ok, ov, t_store = stored if stored is not None else oracle_store(case)
+    done_seqs, done_ctx, t_dec = 0, 0, 0.0
+    H = case.num_heads
+    chunk = 8
+    b = 0
+    while b < case.num_seqs and t_dec < seconds:
+        sel = list(range(b, min(b + chunk, case.num_seqs)))
+        pairs = np.array([s * H + h for s in sel for h in range(H)], np.int64)
+        t0 = time.perf_counter()
+        oracle.decode(case.q, ok, ov, case.block_tables, case.context_lens, pairs=pairs,
+                      nthreads=threads)
+        t_dec += time.perf_counter() - t0
+        done_seqs += len(sel)
+        done_ctx += int(case.context_lens[sel].astype(np.int64).sum())
+        b += chunk
+    kv = done_ctx * case.num_kv_heads * case.head_dim * 4
+    return {"seqs_per_s": done_seqs / t_dec, "gbs": kv / t_dec / 1e9, "cores": cores,
+            "sample": f"{done_seqs} of {case.num_seqs} sequences (all {H} heads), "
+                      f"{done_ctx} context tokens, fp64 oracle, {t_dec:.1f} s decode + "
+                      f"{t_store:.1f} s store of the step on the host"}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores (no reference implementation
+    exists to install). Only rank 0 works."""
+    rank = int(os.environ.get("RANK", 0))
+    if rank != 0:
+        return
+    from paged_kv_cache_107_gb300 import workloads
+    case = workloads.workload(args.workload, poison=False)
+    tot_ctx, kv_bytes, _, _ = workload_summary(case)
+    vals = []
+    base = None
+    stored = oracle_store(case)
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(case, seconds=args.ref_seconds, stored=stored)
+        if i >= args.warmup:
+            vals.append(r["gbs"])
+            base = r
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": kv_bytes / (v * 1e9) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case.name, "num_seqs": case.num_seqs,
+                   "total_context_tokens": tot_ctx},
+        "seqs_per_s": base["seqs_per_s"],
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": base["cores"], "kind": "oracle",
+                         "sample": base["sample"]},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300 import workloads
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk.load_library()
+    case = workloads.workload(args.workload, poison=True, num_blocks=args.pool_blocks)
+    tot_ctx, kv_bytes, small_bytes, store_bytes = workload_summary(case)
+    B, H, Hk, D = case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim
+
+    k_cache = case.k_cache.to(dev)
+    v_cache = case.v_cache.to(dev)
+    q = case.q.to(dev)
+    k_new = case.k_new.to(dev)
+    v_new = case.v_new.to(dev)
+    slots = torch.from_numpy(case.slot_mapping).to(dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    ctx = torch.from_numpy(case.context_lens).to(dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pk.DecodeWorkspace(B, H, Hk, D, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pk.pa_store_kvcache(k_new, v_new, k_cache, v_cache, slots, dev_err=err, stream=stream)
+        pk.pa_decode(out, q, k_cache, v_cache, bt, ctx, workspace=ws, dev_err=err, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} during warm-up")
+
+    # ---- device-timed region: K steps back to back, per-kernel events on the stream ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            pk.pa_store_kvcache(k_new, v_new, k_cache, v_cache, slots, dev_err=err, stream=stream)
+            e1.record(stream)
+            pk.pa_decode(out, q, k_cache, v_cache, bt, ctx, workspace=ws, dev_err=err,
+                         stream=stream)
+            e2.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    store_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev)
+    decode_ms = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev)
+    clk = clocks.summary()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} in the timed region")
+
+    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    seqs_per_s = world * B / (ms_step * 1e-3)
+    hbm_peak, _, peak_src = measured_peaks()
+    decode_alg_bytes = kv_bytes + small_bytes
+    achieved = decode_alg_bytes / (decode_ms * 1e-3) / 1e9
+    traffic = kernel_traffic("decode.cu", "decode_w2_qwen3_b256.md")
+
+    # ---- end to end through the public API with host buffers ---------------------------
+    pin = lambda t: t.pin_memory()
+    h_q, h_k, h_v = pin(case.q), pin(case.k_new), pin(case.v_new)
+    h_slots = pin(torch.from_numpy(case.slot_mapping))
+    h_bt = pin(torch.from_numpy(case.block_tables))
+    h_ctx = pin(torch.from_numpy(case.context_lens))
+    h_out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        k_new.copy_(h_k, non_blocking=True)
+        v_new.copy_(h_v, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        ctx.copy_(h_ctx, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world)
+    barrier(world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": case.name, "num_seqs": B, "num_heads": H, "num_kv_heads": Hk,
+                   "head_dim": D, "block_size": case.block_size, "num_blocks": case.num_blocks,
+                   "total_context_tokens": tot_ctx, "kv_bytes_per_step": kv_bytes,
+                   "l2": "inputs larger than L2 (K/V read per step >> 129 MB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "seqs_per_s": seqs_per_s,
+        "pct_of_nominal_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "pct_of_measured_hbm": 100.0 * value / world / hbm_peak,
+        "kernels_ms": {"store": store_ms, "decode": decode_ms},
+        "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "peak_source": f"{peak_src} HBM copy GB/s",
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "alg_bytes_per_launch": decode_alg_bytes},
+        "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline(case, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cb["gbs"], "unit": "GB/s", "cores": cb["cores"],
+                                "kind": "oracle", "sample": cb["sample"],
+                                "seqs_per_s": cb["seqs_per_s"]}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=1.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-blocks", type=int, default=None,
+                    help="override the block pool size (a smaller pool for profiler captures)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+"""paged_kv_cache_107_gb300 — paged-KV attention for GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``lib/libpagedkv.so`` (declared in
+``include/pa.h``). Every function marshals torch tensors into pointers and sizes and
+calls the library with the same name; all arithmetic runs in the library's CUDA
+kernels. There is no CPU or PyTorch fallback: if the library is missing or a CUDA device
+is absent the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = ["pa_store_kvcache", "pa_decode", "pa_decode_workspace_size", "pa_prefill_varlen",
+           "pa_status_str", "pa_version", "DecodeWorkspace", "library_path", "load_library",
+           "PA_DEV_ERR"]
+
+PA_DEV_ERR = {"block_id": 1, "slot": 2, "context": 4, "timeout": 8, "seqlens": 16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedAttentionError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: Optional[str] = None):
+    """Load (once) the CUDA library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise PagedAttentionError(
+                f"CUDA library not found at {p}; build it first "
+                "(python -m paged_kv_cache_107_gb300.build or __graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        lib.pa_status_str.argtypes = [i32]
+        lib.pa_status_str.restype = ctypes.c_char_p
+        lib.pa_version.argtypes = []
+        lib.pa_version.restype = i32
+        lib.pa_store_kvcache.argtypes = [vp, vp, i64, i64, vp, vp, vp, i32, i32, i32, i32, i64,
+                                         vp, vp]
+        lib.pa_store_kvcache.restype = i32
+        lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.pa_decode_workspace_size.restype = sz
+        lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32,
+                                  i32, vp, sz, vp, vp]
+        lib.pa_decode.restype = i32
+        lib.pa_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                          i32, i32, i64, i32, f32, vp, vp]
+        lib.pa_prefill_varlen.restype = i32
+        _lib = lib
+        return lib
+
+
+def pa_status_str(status: int) -> str:
+    return load_library().pa_status_str(int(status)).decode()
+
+
+def pa_version() -> int:
+    return int(load_library().pa_version())
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise PagedAttentionError(f"{what}: {pa_status_str(rc)}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: Optional[int] = None):
+    if not t.is_cuda:
+        raise PagedAttentionError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise PagedAttentionError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise PagedAttentionError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def pa_store_kvcache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                     dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """k, v [N, Hk, D] bf16 (token stride may exceed Hk*D); caches [nb, bs, Hk, D]."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    nb, bs, hk, d = k_cache.shape
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and v_cache.shape == k_cache.shape):
+        raise PagedAttentionError("caches must be contiguous and of equal shape")
+    for name, t in (("k", k), ("v", v)):
+        if t.shape[1:] != (hk, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise PagedAttentionError(f"{name} rows must be [Hk, D] contiguous")
+    if slot_mapping.shape[0] != k.shape[0] or v.shape[0] != k.shape[0]:
+        raise PagedAttentionError("slot_mapping / k / v token counts differ")
+    rc = load_library().pa_store_kvcache(
+        _ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache), _ptr(v_cache),
+        _ptr(slot_mapping), k.shape[0], hk, d, bs, nb, _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_store_kvcache")
+
+
+def pa_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,
+                             head_dim: int = 128) -> int:
+    return int(load_library().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads,
+                                                       head_dim))
+
+
+class DecodeWorkspace:
+    """Zero-initialised decode scratch (its arrival counters must start at zero; every
+    successful call leaves them zero). One workspace per stream of concurrent calls."""
+
+    def __init__(self, num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int = 128,
+                 device=None):
+        n = pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim)
+        if n == 0:
+            raise PagedAttentionError("invalid decode workspace sizes")
+        self.nbytes = n
+        self.buffer = torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+        self.key = (num_seqs, num_heads, num_kv_heads, head_dim)
+
+    def fits(self, num_seqs, num_heads, num_kv_heads, head_dim=128) -> bool:
+        return pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim) <= self.nbytes
+
+    def reset(self):
+        self.buffer.zero_()
+
+
+_ws_cache = {}
+
+
+def _default_workspace(B, H, Hk, D, device) -> DecodeWorkspace:
+    key = (device.index if device.index is not None else torch.cuda.current_device(), H, Hk, D)
+    ws = _ws_cache.get(key)
+    if ws is None or not ws.fits(B, H, Hk, D):
+        ws = DecodeWorkspace(max(B, 1), H, Hk, D, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor,
+              scale: Optional[float] = None, grid_ctas: int = 0,
+              workspace: Optional[DecodeWorkspace] = None,
+              dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out, q [B, H, D] bf16; caches [nb, bs, Hk, D]; block_tables [B, maxb] int32 (-1
+    padded); context_lens [B] int32."""
+    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
+                            ("k_cache", k_cache, torch.bfloat16, 4),
+                            ("v_cache", v_cache, torch.bfloat16, 4),
+                            ("block_tables", block_tables, torch.int32, 2),
+                            ("context_lens", context_lens, torch.int32, 1)):
+        _need(t, name, dt, nd)
+        if not t.is_contiguous():
+            raise PagedAttentionError(f"{name} must be contiguous")
+    B, H, D = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != D or v_cache.shape != k_cache.shape:
+        raise PagedAttentionError("shape mismatch")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise PagedAttentionError("block_tables / context_lens batch mismatch")
+    if workspace is None:
+        workspace = _default_workspace(B, H, hk, D, q.device)
+    rc = load_library().pa_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, H, hk, D, bs, nb,
+        float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(workspace.buffer),
+        workspace.nbytes, _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_decode")
+    return out
+
+
+def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
+                      max_seqlen_k: int, causal: bool = True, scale: Optional[float] = None,
+                      dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out, q [sum n, H, D] bf16; caches hold every key/value row already (store first)."""
+    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
+                            ("k_cache", k_cache, torch.bfloat16, 4),
+                            ("v_cache", v_cache, torch.bfloat16, 4),
+                            ("block_tables", block_tables, torch.int32, 2),
+                            ("cu_seqlens_q", cu_seqlens_q, torch.int32, 1),
+                            ("cu_seqlens_k", cu_seqlens_k, torch.int32, 1)):
+        _need(t, name, dt, nd)
+        if not t.is_contiguous():
+            raise PagedAttentionError(f"{name} must be contiguous")
+    T, H, D = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    S = cu_seqlens_q.shape[0] - 1
+    if out.shape != q.shape or d2 != D or v_cache.shape != k_cache.shape:
+        raise PagedAttentionError("shape mismatch")
+    if cu_seqlens_k.shape[0] != S + 1 or block_tables.shape[0] != S:
+        raise PagedAttentionError("cu_seqlens / block_tables batch mismatch")
+    rc = load_library().pa_prefill_varlen(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S, int(max_seqlen_q),
+        int(max_seqlen_k), H, hk, D, bs, nb, 1 if causal else 0,
+        float(scale) if scale is not None else 0.0, _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_prefill_varlen")
+    return out

@@ -1,0 +1,189 @@
+// pa_api.cu — the exported C ABI (include/pa.h): argument validation, then launch.
+// Nothing here allocates device memory or synchronises the host.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_launch.h"
+
+namespace pa {
+
+bool current_device_info(DeviceInfo* info) {
+  static DeviceInfo cache[64];
+  static bool valid[64] = {false};
+  static std::mutex mu;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!valid[dev]) {
+    DeviceInfo d{};
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return false;
+    cache[dev] = d;
+    valid[dev] = true;
+  }
+  *info = cache[dev];
+  return true;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static float resolve_scale(float scale, int head_dim) {
+  if (!(scale > 0.f) || isnan(scale)) scale = 1.0f / sqrtf((float)head_dim);
+  return scale * 1.4426950408889634f;  // exp(x) = exp2(x * log2(e))
+}
+
+}  // namespace pa
+
+extern "C" {
+
+const char* pa_status_str(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: inconsistent sizes";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head_dim, group size or block size not supported";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: decode workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime error";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    default: return "unknown pa status";
+  }
+}
+
+int pa_version(void) { return (1 << 16) | 0; }
+
+int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t v_tok_stride,
+                     void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
+                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                     int* dev_err, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_SHAPE;
+  if (head_dim != pa::kHeadDimApi) return PA_ERR_UNSUPPORTED;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (k_tok_stride < row || v_tok_stride < row) return PA_ERR_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_NULL;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
+  return pa::launch_store_kvcache(k, v, k_tok_stride, v_tok_stride, k_cache, v_cache,
+                                  slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                  num_blocks * (int64_t)block_size, dev_err,
+                                  static_cast<cudaStream_t>(stream), info.num_sms);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim != pa::kHeadDimApi)
+    return 0;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return 0;
+  size_t a, b, c, total;
+  pa::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, pa::decode_max_ctas(info), &a,
+                              &b, &c, &total);
+  return total;
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+              size_t workspace_bytes, int* dev_err, void* stream) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq < 0 || grid_ctas < 0)
+    return PA_ERR_SHAPE;
+  if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+  if (head_dim != pa::kHeadDimApi || !pa::decode_supported(num_heads, num_kv_heads))
+    return PA_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens) return PA_ERR_NULL;
+  if (max_blocks_per_seq > 0 && !block_tables) return PA_ERR_NULL;
+  if (!pa::aligned16(out) || !pa::aligned16(q) || !pa::aligned16(k_cache) ||
+      !pa::aligned16(v_cache))
+    return PA_ERR_ALIGN;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
+  const int max_ctas = pa::decode_max_ctas(info);
+  if (grid_ctas == 0) grid_ctas = info.num_sms;
+  if (grid_ctas > max_ctas) return PA_ERR_SHAPE;
+  size_t off_c, off_l, off_o, total;
+  pa::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, max_ctas, &off_c, &off_l,
+                              &off_o, &total);
+  if (!workspace || workspace_bytes < total) return PA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return PA_ERR_ALIGN;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  pa::DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale_log2 = pa::resolve_scale(scale, head_dim);
+  a.grid_ctas = grid_ctas;
+  a.counters = reinterpret_cast<int*>(ws + off_c);
+  a.part_lse = reinterpret_cast<float*>(ws + off_l);
+  a.part_o = reinterpret_cast<float*>(ws + off_o);
+  a.dev_err = dev_err;
+  return pa::launch_decode(a, info, static_cast<cudaStream_t>(stream));
+}
+
+int pa_prefill_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
+                      int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, int causal, float scale,
+                      int* dev_err, void* stream) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || max_blocks_per_seq < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return PA_ERR_SHAPE;
+  if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
+  if (head_dim != pa::kHeadDimApi ||
+      !pa::prefill_supported(num_heads, num_kv_heads, block_size))
+    return PA_ERR_UNSUPPORTED;
+  if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (max_seqlen_k > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_SHAPE;
+  if (num_seqs == 0 || max_seqlen_q == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k) return PA_ERR_NULL;
+  if (max_blocks_per_seq > 0 && !block_tables) return PA_ERR_NULL;
+  if (!pa::aligned16(out) || !pa::aligned16(q) || !pa::aligned16(k_cache) ||
+      !pa::aligned16(v_cache))
+    return PA_ERR_ALIGN;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
+  pa::PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = pa::resolve_scale(scale, head_dim);
+  a.dev_err = dev_err;
+  return pa::launch_prefill(a, info, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,86 @@
+// pa_launch.h — internal host-side launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+// The only head_dim the kernels are built for.
+constexpr int kHeadDimApi = 128;
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;
+  int cc_major;
+  int cc_minor;
+};
+
+// Cached per-device properties of the current device; returns false on a CUDA error.
+bool current_device_info(DeviceInfo* info);
+
+int launch_store_kvcache(const void* k, const void* v, int64_t k_tok_stride,
+                         int64_t v_tok_stride, void* k_cache, void* v_cache,
+                         const int32_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int64_t num_slots, int* dev_err, cudaStream_t stream,
+                         int num_sms);
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int max_blocks;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  int block_size;
+  int64_t num_blocks;
+  float scale_log2;  // softmax scale * log2(e)
+  int grid_ctas;     // CTAs along the key stream (per head slab)
+  int* counters;     // [num_seqs * num_kv_heads]
+  float* part_o;     // [max_ctas * 2 * num_heads * head_dim]
+  float* part_lse;   // [max_ctas * 2 * num_heads]
+  int* dev_err;
+};
+
+// Maximum CTAs along the key stream that a decode workspace is sized for.
+int decode_max_ctas(const DeviceInfo& info);
+// Workspace layout: byte offsets of the counters, partial LSEs and partial outputs.
+void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int max_ctas,
+                             size_t* off_counters, size_t* off_lse, size_t* off_o,
+                             size_t* total);
+// Head slab (KV heads handled by one CTA) for a given num_kv_heads: 8, 4, 2 or 1.
+int decode_head_slab(int num_kv_heads);
+bool decode_supported(int num_heads, int num_kv_heads);
+int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int max_blocks;
+  int num_seqs;
+  int max_seqlen_q;
+  int max_seqlen_k;
+  int num_heads;
+  int num_kv_heads;
+  int block_size;
+  int64_t num_blocks;
+  int causal;
+  float scale_log2;
+  int* dev_err;
+};
+
+bool prefill_supported(int num_heads, int num_kv_heads, int block_size);
+int launch_prefill(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream);
+
+}  // namespace pa

@@ -263,8 +263,11 @@ WORKLOADS = {
 }
 
 
-def workload(num: int, block_size: Optional[int] = None, poison: bool = True) -> PagedCase:
-    """Build named workload `num` (1..5). Workload 4 takes block_size 16 or 256."""
+def workload(num: int, block_size: Optional[int] = None, poison: bool = True,
+             num_blocks: Optional[int] = None) -> PagedCase:
+    """Build named workload `num` (1..5). Workload 4 takes block_size 16 or 256.
+    num_blocks overrides the pool size of workloads 2, 3 and 5 (the drawn lengths and the
+    values do not change; only the physical ids do)."""
     seed = SEED_BASE + num
     if num == 1:
         return decode_case([1, 17, 256, 300], 16, 8, 128, 256, num_blocks=16, seed=seed,
@@ -272,12 +275,14 @@ def workload(num: int, block_size: Optional[int] = None, poison: bool = True) ->
     rng = np.random.default_rng(seed)
     if num == 2:
         lens = rng.integers(100, 2048 + 1, size=256)
-        return decode_case(lens, 16, 8, 128, 256, num_blocks=4096, seed=seed + 1000,
-                           poison=poison, max_blocks=8, name="w2_qwen3_decode_b256")
+        return decode_case(lens, 16, 8, 128, 256, num_blocks=num_blocks or 4096,
+                           seed=seed + 1000, poison=poison, max_blocks=8,
+                           name="w2_qwen3_decode_b256")
     if num == 3:
         lens = rng.integers(32768, 131072 + 1, size=8)
-        return decode_case(lens, 32, 8, 128, 256, num_blocks=4096, seed=seed + 1000,
-                           poison=poison, max_blocks=512, name="w3_long_context_b8")
+        return decode_case(lens, 32, 8, 128, 256, num_blocks=num_blocks or 4096,
+                           seed=seed + 1000, poison=poison, max_blocks=512,
+                           name="w3_long_context_b8")
     if num == 4:
         bs = block_size or 256
         lens = np.clip(np.round(rng.lognormal(6.0, 1.0, size=512)), 1, 4096).astype(np.int64)
@@ -288,6 +293,7 @@ def workload(num: int, block_size: Optional[int] = None, poison: bool = True) ->
     if num == 5:
         cached = rng.integers(0, 2048 + 1, size=32)
         new = rng.integers(100, 1024 + 1, size=32)
-        return prefill_case(cached, new, 16, 8, 128, 256, num_blocks=4096, seed=seed + 1000,
-                            poison=poison, causal=True, name="w5_chunked_prefill")
+        return prefill_case(cached, new, 16, 8, 128, 256, num_blocks=num_blocks or 4096,
+                            seed=seed + 1000, poison=poison, causal=True,
+                            name="w5_chunked_prefill")
     raise ValueError(f"no workload {num}")

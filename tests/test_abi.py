@@ -1,0 +1,81 @@
+"""The C-ABI library loads and exports every entry point that include/pa.h declares;
+host-side validation answers without a GPU. No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_107_gb300 as pk
+from paged_kv_cache_107_gb300 import build as lib_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(pa_[a-z_0-9]+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = lib_build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("pa_store_kvcache", "pa_decode", "pa_decode_workspace_size",
+                 "pa_prefill_varlen", "pa_status_str", "pa_version"):
+        assert must in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} missing from {lib_build.LIB_PATH}"
+
+
+def test_binding_has_same_names():
+    for name in declared_functions():
+        assert hasattr(pk, name) or name.endswith("_noalloc"), name
+
+
+def test_status_strings_and_version():
+    pk.load_library()
+    assert pk.pa_status_str(0) == "PA_OK"
+    assert "SHAPE" in pk.pa_status_str(2)
+    assert pk.pa_version() >> 16 == 1
+
+
+def test_validation_without_launch(lib):
+    """Shape errors are caught before any CUDA call, so they answer on a CPU machine too."""
+    lib.pa_decode.restype = ctypes.c_int
+    vp = ctypes.c_void_p(16)
+    # H % Hk != 0
+    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 12, 8, 128, 16, ctypes.c_int64(4),
+                       ctypes.c_float(0), 0, vp, ctypes.c_size_t(1 << 20), None, None)
+    assert rc == 2
+    # head_dim 64
+    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 16, 8, 64, 16, ctypes.c_int64(4),
+                       ctypes.c_float(0), 0, vp, ctypes.c_size_t(1 << 20), None, None)
+    assert rc == 3
+    # store: negative token count, bad stride
+    lib.pa_store_kvcache.restype = ctypes.c_int
+    rc = lib.pa_store_kvcache(vp, vp, ctypes.c_int64(1024), ctypes.c_int64(1024), vp, vp, vp, -1,
+                              8, 128, 16, ctypes.c_int64(4), None, None)
+    assert rc == 2
+    rc = lib.pa_store_kvcache(vp, vp, ctypes.c_int64(10), ctypes.c_int64(1024), vp, vp, vp, 3, 8,
+                              128, 16, ctypes.c_int64(4), None, None)
+    assert rc == 2
+    # zero tokens is a successful no-op without touching CUDA
+    rc = lib.pa_store_kvcache(None, None, ctypes.c_int64(1024), ctypes.c_int64(1024), None, None,
+                              None, 0, 8, 128, 16, ctypes.c_int64(4), None, None)
+    assert rc == 0
+    # prefill: max_seqlen_k beyond what the table maps
+    lib.pa_prefill_varlen.restype = ctypes.c_int
+    rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 256,
+                               ctypes.c_int64(4), 1, ctypes.c_float(0), None, None)
+    assert rc in (2, 3)
