@@ -65,58 +65,120 @@ def kernel_traffic(kernel_src: str, summary: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled during the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Polls NVML (read-only queries through the driver's libnvidia-ml) from a thread about
+    every millisecond, so even a timed region of a few milliseconds gets samples; falls
+    back to `nvidia-smi -lms 200` when NVML cannot be loaded."""
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.out_path = None
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.samples = []
+        self.reason_bits = 0
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self.source = "none"
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+        except Exception:
+            uuid = None
+        ok = False
+        if uuid:
+            for cand in (uuid, "GPU-" + uuid):
+                if nv.nvmlDeviceGetHandleByUUID(cand.encode(), ctypes.byref(handle)) == 0:
+                    ok = True
+                    break
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle)) != 0:
+            raise OSError("no NVML handle")
+        return nv, handle
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            self.out_path = f"/tmp/pa_clocks_{os.getpid()}.csv"
+            nv, h = self._nvml_handle()
+        except OSError:
+            return self._start_smi()
+        self.source = "nvml"
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or getattr(
+            nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._stop = threading.Event()
+
+        def poll():
+            clk = ctypes.c_uint()
+            rs = ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    self.samples.append(float(clk.value))
+                if get_reasons(h, ctypes.byref(rs)) == 0:
+                    self.reason_bits |= int(rs.value)
+                self._stop.wait(0.001)
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+        return self
+
+    def _start_smi(self):
+        self.source = "nvidia-smi"
+        self.out_path = f"/tmp/pa_clocks_{os.getpid()}.csv"
+        try:
             self.fh = open(self.out_path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
-                stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+                ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.source = "none"
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
+        if self.source == "nvml":
+            self._stop.set()
+            self._thread.join(timeout=2)
+        elif self.source == "nvidia-smi":
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40,
+                    "sw_thermal_slowdown": 0x20, "sw_power_cap": 0x4}
+            for line in open(self.out_path):
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    continue
+                for n, v in zip(names, parts[2:6]):
+                    if v.lower().startswith("active"):
+                        self.reason_bits |= bits[n]
+            os.unlink(self.out_path)
 
     def summary(self):
-        if self.proc is None or not self.out_path or not os.path.exists(self.out_path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.out_path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        os.unlink(self.out_path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted(n for b, n in self.REASONS.items() if self.reason_bits & b)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "source": self.source}
 
 
 def dist_setup(n_gpus: int):
@@ -177,7 +239,9 @@ def cpu_baseline(case, seconds: float = 10.0, threads: int = 0, stored=None):
     H = case.num_heads
     chunk = 8
     b = 0
-    while b < case.num_seqs and t_dec < seconds:
+    while t_dec < seconds:
+        if b >= case.num_seqs:
+            b = 0  # whole batch done: go round again until the time budget is used
         sel = list(range(b, min(b + chunk, case.num_seqs)))
         pairs = np.array([s * H + h for s in sel for h in range(H)], np.int64)
         t0 = time.perf_counter()
@@ -189,7 +253,7 @@ def cpu_baseline(case, seconds: float = 10.0, threads: int = 0, stored=None):
         b += chunk
     kv = done_ctx * case.num_kv_heads * case.head_dim * 4
     return {"seqs_per_s": done_seqs / t_dec, "gbs": kv / t_dec / 1e9, "cores": cores,
-            "sample": f"{done_seqs} of {case.num_seqs} sequences (all {H} heads), "
+            "sample": f"{done_seqs} sequence-passes over the {case.num_seqs}-sequence batch (all {H} heads), "
                       f"{done_ctx} context tokens, fp64 oracle, {t_dec:.1f} s decode + "
                       f"{t_store:.1f} s store of the step on the host"}
 
@@ -272,7 +336,7 @@ def run_ours(args):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clocks:
+    with ClockSampler(dev) as clocks:
         start.record(stream)
         for i in range(args.steps):
             e0, e1, e2 = ev[i]
