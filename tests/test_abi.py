@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_binding_has_same_names():
     for name in declared_functions():
-        assert hasattr(pk, name) or name.endswith("_noalloc"), name
+        assert hasattr(pk, name), name
 
 
 def test_status_strings_and_version():
