@@ -152,6 +152,27 @@ __device__ __forceinline__ float head_bcast(const float* vals, int hh, int lane)
   }
 }
 
+// Packed fp32x2 arithmetic (two independent fp32 lanes per instruction).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+// Two bf16 (element 0 in the low half) widened to an fp32 pair.
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 template <int HS, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_kernel(const DecodeArgs a) {
@@ -306,8 +327,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x == x1 - 1 || lt == nb - 1) flags |= kFlagLast;
       if (pb >= x0 && pb + nb <= x1) flags |= kFlagWhole;
 
+      // The rows of a tile are one contiguous run when the slab is every KV head and the
+      // tile sits inside one block: then lane 0 moves K and V with one copy each.
+      const int pos_first = tok0, pos_last = tok0 + count - 1;
+      const bool one_run = slab_off == 0 && row_elems == (int64_t)HS * kHeadDim &&
+                           count > 0 && (pos_first / a.block_size) == (pos_last / a.block_size);
       const uint16_t* src[ROWS_PER_LANE];
       int ok_rows = 0;
+      if (one_run) {
+#pragma unroll
+        for (int k = 0; k < ROWS_PER_LANE; ++k) src[k] = nullptr;
+        const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos_first / a.block_size);
+        if (blk >= 0 && (int64_t)blk < a.num_blocks) {
+          const int64_t rowi = (int64_t)blk * a.block_size + pos_first % a.block_size;
+          if (lane < 2) {
+            src[0] = (lane ? vc : kc) + rowi * row_elems;
+            ok_rows = count;
+          }
+        } else if (lane == 0) {
+          set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
+        }
+      } else {
 #pragma unroll
       for (int k = 0; k < ROWS_PER_LANE; ++k) {
         src[k] = nullptr;
@@ -327,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      }
       }
       const int total_rows = __reduce_add_sync(0xffffffffu, ok_rows);
       const bool first = flags & kFlagFirst;
@@ -352,6 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&ctl.full[s], bytes);
       }
       __syncwarp();
+      if (one_run) {
+        if (src[0] != nullptr)
+          bulk_g2s_hint(st + lane * C::KV_BYTES, src[0], (uint32_t)count * C::ROW, &ctl.full[s],
+                        policy);
+      } else {
 #pragma unroll
       for (int k = 0; k < ROWS_PER_LANE; ++k) {
         const int r = lane + 32 * k;
@@ -360,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = kv ? r - T : r;
           bulk_g2s_hint(st + kv * C::KV_BYTES + t * C::ROW, src[k], C::ROW, &ctl.full[s], policy);
         }
+      }
       }
       if (first && lane == 0) {
         const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) +
@@ -385,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = bfly_base<C::NV>(sub);
   float* pbuf = pbuf_all + warp * C::PBUF_FLOATS;
 
-  float qf[G][8];
-  float o[G][8];
+  float2 qp[G][4];  // q of the group's heads, this lane's 8 dims, pre-scaled
+  float2 op[G][4];  // running output, this lane's 8 dims
   float m_run[G];
   float m_own[C::CF];
   float l_loc[C::CF];
@@ -394,10 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int hh = 0; hh < G; ++hh) {
     m_run[hh] = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[hh][e] = 0.f, qf[hh][e] = 0.f;
+    for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = make_float2(0.f, 0.f), qp[hh][c2] = op[hh][c2];
   }
 #pragma unroll
   for (int r = 0; r < C::CF; ++r) m_own[r] = -INFINITY, l_loc[r] = 0.f;
+  const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
 
   int seg_count = 0;
   for (int64_t it = 0; it < n_tiles; ++it) {
@@ -417,38 +465,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* Qst = Kst + 2 * C::KV_BYTES;
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        const uint4 qv = lds128(Qst + ((j * G + hh) * kHeadDim + sub * 8) * 2);
-        bf16x8_to_f32(qv, qf[hh]);
+        const uint4 qv = *reinterpret_cast<const uint4*>(Qst + ((j * G + hh) * kHeadDim + sub * 8) * 2);
+        qp[hh][0] = mul2(bf16x2_f2(qv.x), scale2);
+        qp[hh][1] = mul2(bf16x2_f2(qv.y), scale2);
+        qp[hh][2] = mul2(bf16x2_f2(qv.z), scale2);
+        qp[hh][3] = mul2(bf16x2_f2(qv.w), scale2);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qf[hh][e] *= a.scale_log2;
-          o[hh][e] = 0.f;
-        }
+        for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = make_float2(0.f, 0.f);
         m_run[hh] = -INFINITY;
       }
 #pragma unroll
       for (int r = 0; r < C::CF; ++r) m_own[r] = -INFINITY, l_loc[r] = 0.f;
     }
 
-    // ---- scores: q . k for this warp's 8 tokens, reduced over the 16 lanes of a row ----
-    float sc[C::NV];
+    // ---- this warp's rows of the tile: K now, V early (in-bounds shared loads) ---------
+    uint4 kraw[kPairs], vraw[kPairs];
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
       const int t = w * kTokPerWarp + 2 * i + half;
-      float kf[8];
-      if (t < count) {
-        const uint4 kv = lds128(Kst + (t * HS + j) * (kHeadDim * 2) + sub * 16);
-        bf16x8_to_f32(kv, kf);
-      } else {
+      const size_t off = (size_t)(t * HS + j) * (kHeadDim * 2) + sub * 16;
+      kraw[i] = *reinterpret_cast<const uint4*>(Kst + off);
+      vraw[i] = *reinterpret_cast<const uint4*>(Vst + off);
+      if (t >= count) vraw[i] = make_uint4(0u, 0u, 0u, 0u);  // stale rows must not reach p*v
+    }
+
+    // ---- scores: q . k, 8 dims per lane, reduced over the 16 lanes of a row ------------
+    float sc[C::NV];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) kf[e] = 0.f;
-      }
+    for (int i = 0; i < kPairs; ++i) {
+      const float2 k0 = bf16x2_f2(kraw[i].x), k1 = bf16x2_f2(kraw[i].y);
+      const float2 k2 = bf16x2_f2(kraw[i].z), k3 = bf16x2_f2(kraw[i].w);
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        float acc = qf[hh][0] * kf[0];
-#pragma unroll
-        for (int e = 1; e < 8; ++e) acc = fmaf(qf[hh][e], kf[e], acc);
-        sc[i * G + hh] = acc;
+        float2 acc = mul2(qp[hh][0], k0);
+        acc = fma2(qp[hh][1], k1, acc);
+        acc = fma2(qp[hh][2], k2, acc);
+        acc = fma2(qp[hh][3], k3, acc);
+        sc[i * G + hh] = acc.x + acc.y;
       }
     }
     bfly<C::NV>(sc, sub, 8);
@@ -496,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float pv[kPairs * G];
 #pragma unroll
     for (int k = 0; k < kPairs * G / 4; ++k) {
-      const float4 f = lds128f(pbuf + half * kPairs * G + 4 * k);
+      const float4 f = *reinterpret_cast<const float4*>(pbuf + half * kPairs * G + 4 * k);
       pv[4 * k + 0] = f.x;
       pv[4 * k + 1] = f.y;
       pv[4 * k + 2] = f.z;
@@ -505,34 +558,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (rescale) {
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh)
+      for (int hh = 0; hh < G; ++hh) {
+        const float2 al2 = make_float2(alpha[hh], alpha[hh]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[hh][e] *= alpha[hh];
+        for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = mul2(op[hh][c2], al2);
+      }
     }
     // ---- o += p v ----------------------------------------------------------------------
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
-      const int t = w * kTokPerWarp + 2 * i + half;
-      if (t < count) {
-        const uint4 vv = lds128(Vst + (t * HS + j) * (kHeadDim * 2) + sub * 16);
-        float vf[8];
-        bf16x8_to_f32(vv, vf);
+      const float2 v0 = bf16x2_f2(vraw[i].x), v1 = bf16x2_f2(vraw[i].y);
+      const float2 v2 = bf16x2_f2(vraw[i].z), v3 = bf16x2_f2(vraw[i].w);
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const float p = pv[i * G + hh];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(p, vf[e], o[hh][e]);
-        }
+      for (int hh = 0; hh < G; ++hh) {
+        const float2 p2 = make_float2(pv[i * G + hh], pv[i * G + hh]);
+        op[hh][0] = fma2(p2, v0, op[hh][0]);
+        op[hh][1] = fma2(p2, v1, op[hh][1]);
+        op[hh][2] = fma2(p2, v2, op[hh][2]);
+        op[hh][3] = fma2(p2, v3, op[hh][3]);
       }
     }
 
     if (meta.flags & kFlagLast) {
       // ---- finalize the segment ----------------------------------------------------
       // (1) fold the two half-warps (tokens 2i and 2i+1) and total the softmax sums
+      float o[G][8];
 #pragma unroll
       for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[hh][e] += __shfl_xor_sync(0xffffffffu, o[hh][e], 16);
+        for (int c2 = 0; c2 < 4; ++c2) {
+          o[hh][2 * c2] = op[hh][c2].x + __shfl_xor_sync(0xffffffffu, op[hh][c2].x, 16);
+          o[hh][2 * c2 + 1] = op[hh][c2].y + __shfl_xor_sync(0xffffffffu, op[hh][c2].y, 16);
+        }
       float lt[C::CF];
 #pragma unroll
       for (int r = 0; r < C::CF; ++r) {
