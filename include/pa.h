@@ -138,6 +138,37 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               size_t workspace_bytes, int* dev_err, void* stream);
 
 /*
+ * pa_decode_noalloc — pa_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is an interface convenience of the library.
+ *
+ * pa_decode needs a caller-provided workspace. Some callers cannot create one: code
+ * running where no device allocator is available or allowed (a plugin inside a host
+ * program that owns all device memory, a runtime that forbids allocation after start-up,
+ * a caller with a fixed memory budget). This entry point computes exactly what pa_decode
+ * computes with the same arguments, minus workspace/workspace_bytes, and allocates
+ * nothing: its scratch is one fixed array of 16 MiB in the library's device memory, held
+ * by every GPU that loads the library until the process exits.
+ *
+ *   Limit           the scratch needed is round256(num_seqs*num_kv_heads*4)
+ *                   + round256(G*2*num_heads*4) + round256(G*2*num_heads*128*4) bytes,
+ *                   G = grid_ctas (0 = the SM count); more than 16 MiB returns
+ *                   PA_ERR_WORKSPACE and launches nothing.
+ *   First call      the first call on a device looks up the array's device address
+ *                   (cudaGetSymbolAddress, with that device current); make that first
+ *                   call before any stream capture.
+ *   Sharing         every call on a device uses the same array and it keeps the last
+ *                   call's contents; each call clears the arrival counters with an
+ *                   asynchronous memset on `stream` before its launch. Calls that overlap
+ *                   on the GPU (other streams, or in flight together) race on the array:
+ *                   serialise them.
+ */
+int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs, int num_heads,
+                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                      float scale, int grid_ctas, int* dev_err, void* stream);
+
+/*
  * pa_prefill_varlen — causal (or full) varlen attention of new tokens over the paged
  * cache, on the tcgen05 tensor cores.
  * Source: "nano-vllm解读", section "如何适配不同请求不同序列长度" (q [sum_seq_lens, H, d];

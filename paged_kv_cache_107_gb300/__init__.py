@@ -223,3 +223,41 @@ def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         float(scale) if scale is not None else 0.0, _ptr(dev_err), _stream(stream))
     _check(rc, "pa_prefill_varlen")
     return out
+
+
+def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: Optional[float] = None,
+                      grid_ctas: int = 0, dev_err: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """pa_decode for callers that cannot allocate device memory: same arguments without a
+    workspace; the library's fixed 16 MiB device scratch is used instead (see pa.h for the
+    size limit and for why overlapping calls must be serialised)."""
+    lib = load_library()
+    fn = lib.pa_decode_noalloc
+    if not getattr(fn, "_pa_typed", False):
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        fn.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32, i32, vp,
+                       vp]
+        fn.restype = ctypes.c_int
+        fn._pa_typed = True
+    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
+                            ("k_cache", k_cache, torch.bfloat16, 4),
+                            ("v_cache", v_cache, torch.bfloat16, 4),
+                            ("block_tables", block_tables, torch.int32, 2),
+                            ("context_lens", context_lens, torch.int32, 1)):
+        _need(t, name, dt, nd)
+        if not t.is_contiguous():
+            raise PagedAttentionError(f"{name} must be contiguous")
+    B, H, D = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != D or v_cache.shape != k_cache.shape:
+        raise PagedAttentionError("shape mismatch")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise PagedAttentionError("block_tables / context_lens batch mismatch")
+    rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), B, H, hk, D, bs, nb,
+            float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(dev_err),
+            _stream(stream))
+    _check(rc, "pa_decode_noalloc")
+    return out
