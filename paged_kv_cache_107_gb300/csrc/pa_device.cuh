@@ -10,9 +10,9 @@
 namespace pa {
 
 constexpr int kHeadDim = 128;
-// try_wait iterations before a wait is declared stuck (each try may suspend briefly in
-// hardware, so this bounds a broken pipeline to seconds, never forever).
-constexpr uint32_t kWaitLimit = 1u << 22;
+// SM clock cycles before a wait is declared stuck (about 0.13 s at 2 GHz; a healthy wait in
+// these pipelines lasts microseconds), so a broken pipeline ends instead of hanging.
+constexpr long long kWaitCycles = 1ll << 28;
 
 __device__ __forceinline__ void set_dev_err(int* dev_err, int bit) {
   if (dev_err) atomicOr(dev_err, bit);
@@ -58,8 +58,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // phase did not complete within the limit; *abort makes later waits give up at once.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint32_t limit = (abort && *abort) ? 64u : kWaitLimit;
-  for (uint32_t i = 0; i < limit; ++i) {
+  const long long limit = (abort && *abort) ? 4096ll : kWaitCycles;
+  const long long t0 = clock64();
+  while (clock64() - t0 < limit) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
