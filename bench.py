@@ -292,6 +292,73 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def prefill_flops(case) -> float:
+    """4*H*D per unmasked (query, key) pair: sum over sequences of sum_i (c_s + i + 1)."""
+    import numpy as np
+    n = np.diff(case.cu_seqlens_q).astype(np.float64)
+    k = np.diff(case.cu_seqlens_k).astype(np.float64)
+    c = k - n
+    if case.causal:
+        pairs = float(np.sum(n * c + n * (n + 1) / 2))
+    else:
+        pairs = float(np.sum(n * k))
+    return 4.0 * case.num_heads * case.head_dim * pairs
+
+
+def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None):
+    """Chunked-prefill step of workload 5: store of every new token, then causal prefill.
+    Returns timings (CUDA events on the stream), TFLOP/s and the fraction of the measured
+    sustained bf16 tensor peak."""
+    import torch
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300 import workloads
+    case = workloads.workload(5, poison=True, num_blocks=pool_blocks)
+    kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+    q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+    slots = torch.from_numpy(case.slot_mapping).to(dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    cu_q = torch.from_numpy(case.cu_seqlens_q).to(dev)
+    cu_k = torch.from_numpy(case.cu_seqlens_k).to(dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def store():
+        pk.pa_store_kvcache(kn, vn, kc, vc, slots, dev_err=err, stream=stream)
+
+    def prefill():
+        pk.pa_prefill_varlen(out, q, kc, vc, bt, cu_q, cu_k, case.max_seqlen_q, case.max_seqlen_k,
+                             causal=True, dev_err=err, stream=stream)
+
+    for _ in range(max(warmup, 3)):
+        store()
+        prefill()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        store()
+        e1.record(stream)
+        prefill()
+        e2.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} in prefill")
+    st_ms = statistics.median(a.elapsed_time(b) for a, b, _ in ev)
+    pf_ms = statistics.median(b.elapsed_time(c) for _, b, c in ev)
+    flops = prefill_flops(case)
+    _, tflops_peak, src = measured_peaks()
+    nq = int(case.cu_seqlens_q[-1])
+    store_bytes = nq * case.num_kv_heads * case.head_dim * 2 * 2 * 2
+    return {"workload": case.name, "new_tokens": nq, "flops": flops,
+            "prefill_ms": pf_ms, "store_ms": st_ms,
+            "tflops": flops / (pf_ms * 1e-3) / 1e12,
+            "tflops_frac": flops / (pf_ms * 1e-3) / 1e12 / tflops_peak,
+            "peak_tflops": tflops_peak, "peak_source": f"{src} bf16 dense (sustained)",
+            "tokens_per_s": nq / (pf_ms * 1e-3),
+            "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -421,6 +488,8 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
+    if not args.no_prefill:
+        line["prefill"] = measure_prefill(dev, steps=min(args.steps, 20), warmup=args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(case, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["gbs"], "unit": "GB/s", "cores": cb["cores"],
@@ -443,11 +512,22 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=1.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the secondary chunked-prefill measurement")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the chunked-prefill step (for profiler captures)")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="override the block pool size (a smaller pool for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_prefill(dev, args.steps, args.warmup, args.pool_blocks)))
     else:
         run_ours(args)
 

@@ -8,24 +8,27 @@
 // h, over keys t <= c_s + i (causal) or all k_s keys, read through block_tables[s]:
 // o = softmax(scale * q K^T) V.
 //
-// GB300 design (one CTA per (KV head j, sequence s, 128-row query tile)):
-//  * The 128 rows of a query tile are 128/G positions x the G query heads of KV group j
-//    (G = H/H_kv), so every K/V tile fetched for the group serves all of its heads.
+// GB300 design (one CTA per (KV head j, sequence s, pair of 128-row query tiles)):
+//  * A 128-row query tile is 128/G positions x the G query heads of KV group j (G = H/H_kv),
+//    so every K/V tile fetched for the group serves all of its heads. A CTA holds two such
+//    tiles (A: the earlier positions, B: the next ones) that take turns on the tensor core,
+//    so one softmax warpgroup works while the other's products run.
 //  * TMA: K and V are described by 4-D tensor maps over [num_blocks, block_size, H_kv, D];
-//    a box of (64 dims x 1 head x R rows x 1 block), 128-byte swizzled, takes the
-//    physical block id straight from the block table as a coordinate, so a 128-key tile is
-//    2 boxes (R = 128 when block_size >= 128) or 2*(128/block_size) boxes.
+//    a box of (64 dims x 1 head x R rows x 1 block), 128-byte swizzled, takes the physical
+//    block id from the block table as a coordinate. A K/V tile is 64 keys (R = 64 when
+//    block_size >= 64, else several blocks), staged through a 4-deep ring.
 //  * tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor memory):
-//    S = Q K^T (A = Q, B = K, both K-major) into one of two S buffers (256 columns), then
-//    O += P V (A = P in shared memory, B = V MN-major) into O (128 columns). One elected
-//    thread issues all MMAs; completion reaches the other warps through tcgen05.commit
-//    on mbarriers. While the softmax warps work on S(i), the tensor core already runs
-//    S(i+1).
-//  * Softmax: 4 warps, thread r owns row r (TMEM lane r): scores are masked by key index
-//    (causal and length), the running max is only moved when it grows by more than 2^8
-//    (then O is rescaled in tensor memory), P is written to shared memory as bf16 in the
-//    128-byte-swizzled K-major layout the MMA reads. Rows past the sequence length of the
-//    last V tile are zeroed so stale or poisoned rows never meet a zero probability.
+//    S = Q K^T (A = Q, B = K, both K-major; two 64-column S buffers per query tile) and
+//    O += P V (A = P, bf16 in shared memory; B = V, MN-major), O in 128 columns per tile:
+//    4 x 64 + 2 x 128 = all 512 columns. One thread issues every MMA; completion reaches the
+//    other warps through tcgen05.commit on mbarriers. Key tiles past the causal limit of
+//    tile A are not multiplied for A.
+//  * Softmax: 8 warps, thread r of a warpgroup owns row r of its tile (TMEM lane r): scores
+//    are masked by key index (causal and length), reduced with tree max/sum, the running max
+//    is only moved when it grows by more than 2^8 (then O is rescaled in tensor memory), and
+//    P is written as bf16 in the 128-byte-swizzled K-major layout the MMA reads. Rows of the
+//    last V tile past the sequence are zeroed, so stale or poisoned rows never meet a zero
+//    probability.
 //  * Every wait is bounded; on a timeout the kernel records PA_DEV_ERR_TIMEOUT, runs to
 //    the end of its protocol and frees its tensor memory.
 #include <cuda.h>
@@ -43,37 +46,35 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = 128;          // query rows per CTA (TMEM lanes)
-constexpr int kKeys = 128;          // keys per K/V tile
-constexpr int kHalfBytes = 128 * 128;  // one 64-dim (or 64-key) column block: 128 rows x 128 B
-constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB: a 128 x 128 bf16 tile
-constexpr int kThreads = 192;       // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kRows = 128;                 // query rows per tile (TMEM lanes)
+constexpr int kKeys = 64;                  // keys per K/V tile
+constexpr int kStages = 4;                 // K/V ring depth
+constexpr int kQHalf = 128 * 128;          // 128 rows x 64 dims (one swizzled column block)
+constexpr int kKVHalf = kKeys * 128;       // 64 rows x 64 dims
+constexpr int kThreads = 320;              // warps 0-3 tile A, 4-7 tile B, 8 TMA, 9 MMA
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM columns: S of tile g, buffer b at g*128 + b*64; O of tile g at 256 + g*128.
+__host__ __device__ constexpr uint32_t col_s(int g, int b) { return (uint32_t)(g * 128 + b * 64); }
+__host__ __device__ constexpr uint32_t col_o(int g) { return (uint32_t)(256 + g * 128); }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows 256x
 
 struct PrefillSmem {
   // 1024-byte aligned tiles (128-byte swizzle atoms are 1024 bytes)
-  unsigned char q[kTileBytes];
-  unsigned char k[2][kTileBytes];
-  unsigned char v[2][kTileBytes];
-  unsigned char p[kTileBytes];
+  unsigned char q[2][2 * kQHalf];          // [tile][dim half]
+  unsigned char p[2][kRows * 128];         // [tile] 128 rows x 64 keys
+  unsigned char k[kStages][2 * kKVHalf];   // [stage][dim half]
+  unsigned char v[kStages][2 * kKVHalf];
   uint64_t q_full;
-  uint64_t k_full[2];
-  uint64_t v_full[2];
-  uint64_t kv_empty[2];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_done;
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2][2];                   // [tile][buffer]
+  uint64_t p_full[2];
+  uint64_t o_done[2];
   uint32_t tmem_base;
   int abort;
 };
-
-// Byte offset of 16-byte chunk `chunk` (0..15) of row `row` in a 128 x 128 bf16 tile stored
-// as two 128-byte-swizzled column blocks (chunks 0..7 and 8..15).
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
-  return (uint32_t)((chunk >> 3) * kHalfBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
-}
 
 __device__ __forceinline__ void note_timeout(PrefillSmem& sm, int* dev_err) {
   sm.abort = 1;
@@ -84,7 +85,7 @@ template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-  constexpr int P = kRows / G;  // query positions per CTA
+  constexpr int P = kRows / G;  // query positions per tile
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -108,26 +109,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   if (n > a.max_seqlen_q && tid == 0 && qt == 0 && j == 0) set_dev_err(a.dev_err, PA_DEV_ERR_SEQLENS);
-  const int i0 = qt * P;
+  const int i0 = qt * 2 * P;
   if (i0 >= n) return;  // nothing to do (before any barrier or tensor memory)
-  const int rows_valid = min(P, n - i0);
-  const int n_keys = a.causal ? (c_len + i0 + rows_valid) : kv_len;
-  const int n_tiles = (n_keys + kKeys - 1) / kKeys;
+  // keys needed by each tile (causal: up to its last position); tile B may be empty
+  int n_tiles[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int rows = min(P, n - (i0 + g * P));
+    const int keys = rows <= 0 ? 0 : (a.causal ? c_len + i0 + g * P + rows : kv_len);
+    n_tiles[g] = (keys + kKeys - 1) / kKeys;
+  }
+  const int n_all = max(n_tiles[0], n_tiles[1]);
 
   if (tid == 0) {
-    mbar_init(&sm.q_full, 128);
-    for (int b = 0; b < 2; ++b) {
+    mbar_init(&sm.q_full, 2 * kRows);
+    for (int b = 0; b < kStages; ++b) {
       mbar_init(&sm.k_full[b], 1);
       mbar_init(&sm.v_full[b], 1);
       mbar_init(&sm.kv_empty[b], 1);
-      mbar_init(&sm.s_full[b], 1);
     }
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.o_done, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&sm.s_full[g][0], 1);
+      mbar_init(&sm.s_full[g][1], 1);
+      mbar_init(&sm.p_full[g], kRows);
+      mbar_init(&sm.o_done[g], 1);
+    }
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     umma::tmem_alloc(&sm.tmem_base, kTmemCols);
     umma::tmem_relinquish();
   }
@@ -137,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       umma::prefetch_tmap(&tm_k);
@@ -146,12 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int box_rows = bs < kKeys ? bs : kKeys;
       const int boxes = kKeys / box_rows;
       const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it & 1;
-        if (it >= 2 && !mbar_wait(&sm.kv_empty[st], (uint32_t)(((it >> 1) - 1) & 1), abort_flag))
+      for (int it = 0; it < n_all; ++it) {
+        const int st = it % kStages;
+        if (it >= kStages &&
+            !mbar_wait(&sm.kv_empty[st], (uint32_t)(((it / kStages) - 1) & 1), abort_flag))
           note_timeout(sm, a.dev_err);
         const int t0 = it * kKeys;
-        int blk[kKeys / 8];  // at most 16 boxes (block_size 8)
+        int blk[kKeys / 8];  // at most 8 boxes (block_size 8)
         uint32_t bytes = 0;
         for (int bx = 0; bx < boxes; ++bx) {
           const int key0 = t0 + bx * box_rows;
@@ -171,108 +182,127 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int bx = 0; bx < boxes; ++bx) {
           if (blk[bx] < 0) continue;
           for (int h2 = 0; h2 < 2; ++h2)
-            umma::tma_load_4d(sm.k[st] + h2 * kHalfBytes + bx * box_rows * 128, &tm_k, h2 * 64, j,
+            umma::tma_load_4d(sm.k[st] + h2 * kKVHalf + bx * box_rows * 128, &tm_k, h2 * 64, j,
                               row0, blk[bx], &sm.k_full[st]);
         }
         mbar_arrive_expect_tx(&sm.v_full[st], bytes);
         for (int bx = 0; bx < boxes; ++bx) {
           if (blk[bx] < 0) continue;
           for (int h2 = 0; h2 < 2; ++h2)
-            umma::tma_load_4d(sm.v[st] + h2 * kHalfBytes + bx * box_rows * 128, &tm_v, h2 * 64, j,
+            umma::tma_load_4d(sm.v[st] + h2 * kKVHalf + bx * box_rows * 128, &tm_v, h2 * 64, j,
                               row0, blk[bx], &sm.v_full[st]);
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma::idesc_bf16_f32(kRows, kKeys, false);
       constexpr uint32_t idesc_o = umma::idesc_bf16_f32(kRows, 128, true);
-      const uint32_t q_addr = smem_u32(sm.q);
-      const uint32_t p_addr = smem_u32(sm.p);
       if (!mbar_wait(&sm.q_full, 0, abort_flag)) note_timeout(sm, a.dev_err);
       umma::fence_after_sync();
       auto issue_pv = [&](int it) {
-        const int st = it & 1;
-        if (!mbar_wait(&sm.p_full, (uint32_t)(it & 1), abort_flag)) note_timeout(sm, a.dev_err);
-        if (!mbar_wait(&sm.v_full[st], (uint32_t)((it >> 1) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
-        umma::fence_after_sync();
+        const int st = it % kStages;
         const uint32_t v_addr = smem_u32(sm.v[st]);
+        bool v_ready = false;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t ad = umma::smem_desc(p_addr + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = umma::smem_desc(v_addr + kk * 16 * 128, kHalfBytes, 1024);
-          umma::mma_bf16(tmem + kColO, ad, bd, idesc_o, (it > 0) || (kk > 0));
+        for (int g = 0; g < 2; ++g) {
+          if (it >= n_tiles[g]) continue;
+          if (!mbar_wait(&sm.p_full[g], (uint32_t)(it & 1), abort_flag)) note_timeout(sm, a.dev_err);
+          if (!v_ready) {
+            if (!mbar_wait(&sm.v_full[st], (uint32_t)((it / kStages) & 1), abort_flag))
+              note_timeout(sm, a.dev_err);
+            v_ready = true;
+          }
+          umma::fence_after_sync();
+          const uint32_t p_addr = smem_u32(sm.p[g]);
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t ad = umma::smem_desc(p_addr + kk * 32, 16, 1024);
+            const uint64_t bd = umma::smem_desc(v_addr + kk * 16 * 128, kKVHalf, 1024);
+            umma::mma_bf16(tmem + col_o(g), ad, bd, idesc_o, (it > 0) || (kk > 0));
+          }
+          umma::commit(&sm.o_done[g]);
         }
         umma::commit(&sm.kv_empty[st]);
-        umma::commit(&sm.o_done);
       };
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it & 1;
-        if (!mbar_wait(&sm.k_full[st], (uint32_t)((it >> 1) & 1), abort_flag))
+      for (int it = 0; it < n_all; ++it) {
+        const int st = it % kStages;
+        if (!mbar_wait(&sm.k_full[st], (uint32_t)((it / kStages) & 1), abort_flag))
           note_timeout(sm, a.dev_err);
         umma::fence_after_sync();
         const uint32_t k_addr = smem_u32(sm.k[st]);
-        const uint32_t s_col = (it & 1) ? kColS1 : kColS0;
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          const uint64_t ad = umma::smem_desc(q_addr + off, 16, 1024);
-          const uint64_t bd = umma::smem_desc(k_addr + off, 16, 1024);
-          umma::mma_bf16(tmem + s_col, ad, bd, idesc_s, kk > 0);
+        for (int g = 0; g < 2; ++g) {
+          if (it >= n_tiles[g]) continue;
+          const uint32_t q_addr = smem_u32(sm.q[g]);
+#pragma unroll
+          for (int kk = 0; kk < 128 / 16; ++kk) {
+            const uint64_t ad = umma::smem_desc(q_addr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = umma::smem_desc(k_addr + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024);
+            umma::mma_bf16(tmem + col_s(g, it & 1), ad, bd, idesc_s, kk > 0);
+          }
+          umma::commit(&sm.s_full[g][it & 1]);
         }
-        umma::commit(&sm.s_full[it & 1]);
         if (it > 0) issue_pv(it - 1);
       }
-      issue_pv(n_tiles - 1);
-      // the last commit must land before tensor memory is released
-      if (!mbar_wait(&sm.o_done, (uint32_t)((n_tiles - 1) & 1), abort_flag))
-        note_timeout(sm, a.dev_err);
+      issue_pv(n_all - 1);
+      // the last products must land before tensor memory is released
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (n_tiles[g] > 0 &&
+            !mbar_wait(&sm.o_done[g], (uint32_t)((n_tiles[g] - 1) & 1), abort_flag))
+          note_timeout(sm, a.dev_err);
     }
   } else {
-    // ------------------------------------------------------------------ softmax warps
-    const int r = tid;  // row == TMEM lane
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int g = warp >> 2;      // query tile of this warpgroup
+    const int r = tid & 127;      // row == TMEM lane
+    const int wq = warp & 3;      // warp within the warpgroup (TMEM lane quarter)
     const int pos = r / G, hh = r % G;
-    const int qi = i0 + pos;             // new-token index within the sequence
+    const int qi = i0 + g * P + pos;     // new-token index within the sequence
     const bool row_ok = qi < n;
     const int qpos = c_len + qi;         // absolute position of this query row
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int lim_row = a.causal ? min(kv_len, qpos + 1) : kv_len;  // keys [0, lim_row) count
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const int nt = n_tiles[g];
 
     // Q row -> shared memory (128-byte swizzled, K-major)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const uint16_t*>(a.q) + ((int64_t)(q0 + qi) * H + j * G + hh) * kHeadDim);
+      uint4 qv[16];
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint4 v = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sm.q + sw128_offset(r, ch)) = v;
-      }
+      for (int ch = 0; ch < 16; ++ch) qv[ch] = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch)
+        *reinterpret_cast<uint4*>(sm.q[g] + (ch >> 3) * kQHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+            qv[ch];
       fence_proxy_async_smem();
       mbar_arrive(&sm.q_full);
     }
 
     float m_run = -INFINITY, l_run = 0.f;
-    float sv[kKeys];
-    for (int it = 0; it < n_tiles; ++it) {
+    for (int it = 0; it < nt; ++it) {
       const int buf = it & 1;
-      if (!mbar_wait(&sm.s_full[buf], (uint32_t)((it >> 1) & 1), abort_flag))
+      if (!mbar_wait(&sm.s_full[g][buf], (uint32_t)((it >> 1) & 1), abort_flag))
         note_timeout(sm, a.dev_err);
       umma::fence_after_sync();
-      const uint32_t s_col = buf ? kColS1 : kColS0;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) umma::tmem_ld32(lane_addr + s_col + 32 * c4, sv + 32 * c4);
+      float sv[kKeys];
+      umma::tmem_ld32(lane_addr + col_s(g, buf), sv);
+      umma::tmem_ld32(lane_addr + col_s(g, buf) + 32, sv + 32);
       umma::tmem_ld_wait();
 
       const int t0 = it * kKeys;
-      const int lim = a.causal ? min(kv_len, qpos + 1) : kv_len;  // keys [t0, lim) count
-      float mt = -INFINITY;
+      float mx[8];
 #pragma unroll
       for (int c = 0; c < kKeys; ++c) {
-        const float x = (t0 + c < lim) ? sv[c] * a.scale_log2 : -INFINITY;
+        const float x = (t0 + c < lim_row) ? sv[c] * a.scale_log2 : -INFINITY;
         sv[c] = x;
-        mt = fmaxf(mt, x);
+        mx[c & 7] = (c < 8) ? x : fmaxf(mx[c & 7], x);
       }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float m_use, alpha;
       bool rescale = false;
       if (it == 0) {
@@ -287,19 +317,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = 1.f;
       }
       const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
-      float rs = 0.f;
+      float sm8[8];
 #pragma unroll
       for (int c = 0; c < kKeys; ++c) {
         const float p = fast_exp2(sv[c] - m_safe);
         sv[c] = p;
-        rs += p;
+        sm8[c & 7] = (c < 8) ? p : sm8[c & 7] + p;
       }
+      const float rs = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
       l_run = l_run * alpha + rs;
       m_run = m_use;
 
-      // O and the P buffer belong to PV(it-1) until it completes
+      // O and the P buffer of this tile belong to PV(it-1) until it completes
       if (it > 0) {
-        if (!mbar_wait(&sm.o_done, (uint32_t)((it - 1) & 1), abort_flag))
+        if (!mbar_wait(&sm.o_done[g], (uint32_t)((it - 1) & 1), abort_flag))
           note_timeout(sm, a.dev_err);
         umma::fence_after_sync();
       }
@@ -307,62 +338,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ob[32];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          umma::tmem_ld32(lane_addr + kColO + 32 * c4, ob);
+          umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob);
           umma::tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) ob[e] *= alpha;
-          umma::tmem_st32(lane_addr + kColO + 32 * c4, ob);
+          umma::tmem_st32(lane_addr + col_o(g) + 32 * c4, ob);
         }
         umma::tmem_st_wait();
       }
       // rows of the last V tile beyond the sequence: zero them (never multiply a stale row)
       if (t0 + kKeys > kv_len) {
-        const int st = it & 1;
-        if (!mbar_wait(&sm.v_full[st], (uint32_t)((it >> 1) & 1), abort_flag))
+        const int st = it % kStages;
+        if (!mbar_wait(&sm.v_full[st], (uint32_t)((it / kStages) & 1), abort_flag))
           note_timeout(sm, a.dev_err);
-        if (r >= kv_len - t0) {
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch)
-            *reinterpret_cast<uint4*>(sm.v[st] + (ch >> 3) * kHalfBytes + r * 128 + (ch & 7) * 16) =
+        const int first_bad = kv_len - t0;
+        for (int idx = r; idx < kKeys * 16; idx += kRows) {
+          const int row = idx >> 4, ch = idx & 15;
+          if (row >= first_bad)
+            *reinterpret_cast<uint4*>(sm.v[st] + (ch >> 3) * kKVHalf + row * 128 + (ch & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // P row (bf16) -> shared memory, 128-byte swizzled K-major
+      // P row (bf16) -> shared memory, 128-byte swizzled K-major (64 keys = one 128 B row)
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 0; ch < 8; ++ch) {
         uint4 pk;
         pk.x = f32x2_to_bf16x2(sv[8 * ch + 0], sv[8 * ch + 1]);
         pk.y = f32x2_to_bf16x2(sv[8 * ch + 2], sv[8 * ch + 3]);
         pk.z = f32x2_to_bf16x2(sv[8 * ch + 4], sv[8 * ch + 5]);
         pk.w = f32x2_to_bf16x2(sv[8 * ch + 6], sv[8 * ch + 7]);
-        *reinterpret_cast<uint4*>(sm.p + sw128_offset(r, ch)) = pk;
+        *reinterpret_cast<uint4*>(sm.p[g] + r * 128 + ((ch ^ (r & 7)) << 4)) = pk;
       }
       fence_proxy_async_smem();
       umma::fence_before_sync();
-      mbar_arrive(&sm.p_full);
+      mbar_arrive(&sm.p_full[g]);
     }
 
     // ---- epilogue: O / l -> bf16 rows ------------------------------------------------
-    if (!mbar_wait(&sm.o_done, (uint32_t)((n_tiles - 1) & 1), abort_flag))
-      note_timeout(sm, a.dev_err);
-    umma::fence_after_sync();
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                          ((int64_t)(q0 + qi) * H + j * G + hh) * kHeadDim);
+    if (nt > 0) {
+      if (!mbar_wait(&sm.o_done[g], (uint32_t)((nt - 1) & 1), abort_flag))
+        note_timeout(sm, a.dev_err);
+      umma::fence_after_sync();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                            ((int64_t)(q0 + qi) * H + j * G + hh) * kHeadDim);
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      float ob[32];
-      umma::tmem_ld32(lane_addr + kColO + 32 * c4, ob);
-      umma::tmem_ld_wait();
-      if (row_ok) {
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float ob[32];
+        umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob);
+        umma::tmem_ld_wait();
+        if (row_ok) {
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint4 pk;
-          pk.x = f32x2_to_bf16x2(ob[8 * q8 + 0] * inv, ob[8 * q8 + 1] * inv);
-          pk.y = f32x2_to_bf16x2(ob[8 * q8 + 2] * inv, ob[8 * q8 + 3] * inv);
-          pk.z = f32x2_to_bf16x2(ob[8 * q8 + 4] * inv, ob[8 * q8 + 5] * inv);
-          pk.w = f32x2_to_bf16x2(ob[8 * q8 + 6] * inv, ob[8 * q8 + 7] * inv);
-          dst[c4 * 4 + q8] = pk;
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 pk;
+            pk.x = f32x2_to_bf16x2(ob[8 * q8 + 0] * inv, ob[8 * q8 + 1] * inv);
+            pk.y = f32x2_to_bf16x2(ob[8 * q8 + 2] * inv, ob[8 * q8 + 3] * inv);
+            pk.z = f32x2_to_bf16x2(ob[8 * q8 + 4] * inv, ob[8 * q8 + 5] * inv);
+            pk.w = f32x2_to_bf16x2(ob[8 * q8 + 6] * inv, ob[8 * q8 + 7] * inv);
+            dst[c4 * 4 + q8] = pk;
+          }
         }
       }
     }
@@ -371,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: every role is done with tensor memory ----------------------------------
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     umma::fence_after_sync();
     umma::tmem_dealloc(tmem, kTmemCols);
   }
@@ -415,6 +449,7 @@ int launch_prefill_t(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t 
                      const CUtensorMap& mk, const CUtensorMap& mv) {
   constexpr int P = kRows / G;
   const size_t smem = sizeof(PrefillSmem) + 1024;
+  static_assert(sizeof(PrefillSmem) + 1024 <= 227 * 1024, "shared memory budget");
   static bool attr_done[64] = {false};
   if (info.device < 0 || info.device >= 64) return PA_ERR_CUDA;
   if (!attr_done[info.device]) {
@@ -423,7 +458,7 @@ int launch_prefill_t(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t 
       return PA_ERR_CUDA;
     attr_done[info.device] = true;
   }
-  const int q_tiles = (a.max_seqlen_q + P - 1) / P;
+  const int q_tiles = (a.max_seqlen_q + 2 * P - 1) / (2 * P);  // pairs of query tiles
   if (q_tiles > 65535) return PA_ERR_UNSUPPORTED;
   dim3 grid((unsigned)a.num_kv_heads, (unsigned)a.num_seqs, (unsigned)q_tiles);
   paged_prefill_kernel<G><<<grid, kThreads, smem, stream>>>(mk, mv, a);
