@@ -294,15 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::tmem_ld_wait();
 
       const int t0 = it * kKeys;
+      // only tiles that reach past this row's last visible key need a mask
+      if (__any_sync(0xffffffffu, t0 + kKeys > lim_row)) {
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c)
+          if (t0 + c >= lim_row) sv[c] = -INFINITY;
+      }
       float mx[8];
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const float x = (t0 + c < lim_row) ? sv[c] * a.scale_log2 : -INFINITY;
-        sv[c] = x;
-        mx[c & 7] = (c < 8) ? x : fmaxf(mx[c & 7], x);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 0; c < 8; ++c) mx[c] = sv[c];
+#pragma unroll
+      for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+      // the scale is positive, so the max of the scaled scores is the scaled max
+      const float mt = a.scale_log2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                            fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float m_use, alpha;
       bool rescale = false;
       if (it == 0) {
@@ -317,14 +322,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = 1.f;
       }
       const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
-      float sm8[8];
+      // p = 2^(s*scale - m): one packed fma per pair of scores, then ex2
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      const float2 nm2 = make_float2(-m_safe, -m_safe);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const float p = fast_exp2(sv[c] - m_safe);
-        sv[c] = p;
-        sm8[c & 7] = (c < 8) ? p : sm8[c & 7] + p;
+      for (int c = 0; c < kKeys / 2; ++c) {
+        const float2 x = umma::ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sc2, nm2);
+        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        sv[2 * c] = p.x;
+        sv[2 * c + 1] = p.y;
+        acc[c & 3] = umma::fadd2(acc[c & 3], p);
       }
-      const float rs = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
+      const float2 t01 = umma::fadd2(acc[0], acc[1]), t23 = umma::fadd2(acc[2], acc[3]);
+      const float2 tt = umma::fadd2(t01, t23);
+      const float rs = tt.x + tt.y;
       l_run = l_run * alpha + rs;
       m_run = m_use;
 
