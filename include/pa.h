@@ -192,8 +192,8 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
  *                   t <= c_s + i. Zero: it sees all k_s keys.
  *   scale           softmax scale; <= 0 or NaN means 1/sqrt(head_dim).
  *
- * Requirements: block_size a multiple of 64, or a divisor of 64 that is a multiple of 8;
- * q, out and both caches 16-byte aligned. Arithmetic: bf16 tensor-core products
+ * Requirements: block_size a multiple of 128, or a divisor of 128 that is a multiple of
+ * 8; q, out and both caches 16-byte aligned. Arithmetic: bf16 tensor-core products
  * with fp32 accumulation, fp32 softmax, P rounded to bf16 for the second product, one
  * bf16 rounding of the output.
  */

@@ -11,24 +11,27 @@
 // GB300 design (one CTA per (KV head j, sequence s, pair of 128-row query tiles)):
 //  * A 128-row query tile is 128/G positions x the G query heads of KV group j (G = H/H_kv),
 //    so every K/V tile fetched for the group serves all of its heads. A CTA holds two such
-//    tiles (A: the earlier positions, B: the next ones) that take turns on the tensor core,
-//    so one softmax warpgroup works while the other's products run.
+//    tiles (A: the earlier positions, B: the next ones) that take turns on the tensor core:
+//    while one softmax warpgroup works, the other tile's products run.
 //  * TMA: K and V are described by 4-D tensor maps over [num_blocks, block_size, H_kv, D];
 //    a box of (64 dims x 1 head x R rows x 1 block), 128-byte swizzled, takes the physical
-//    block id from the block table as a coordinate. A K/V tile is 64 keys (R = 64 when
-//    block_size >= 64, else several blocks), staged through a 4-deep ring.
-//  * tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor memory):
-//    S = Q K^T (A = Q, B = K, both K-major; two 64-column S buffers per query tile) and
-//    O += P V (A = P, bf16 in shared memory; B = V, MN-major), O in 128 columns per tile:
-//    4 x 64 + 2 x 128 = all 512 columns. One thread issues every MMA; completion reaches the
-//    other warps through tcgen05.commit on mbarriers. Key tiles past the causal limit of
+//    block id from the block table as a coordinate. A K/V tile is 128 keys (R = 128 when
+//    block_size >= 128, else several blocks). K has a 3-deep ring, V a 2-deep one; K runs
+//    one tile ahead of V.
+//  * tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor memory, all 512
+//    columns): S_g = Q_g K^T (A = Q and B = K from shared memory, K-major) in 128 columns per
+//    tile; the softmax writes P back over S as packed bf16 and O_g += P V reads P straight
+//    from tensor memory (B = V, MN-major) into 128 more columns per tile. On the tensor core
+//    the order per key tile is PV_A(i), S_A(i+1), PV_B(i), S_B(i+1): each S is issued only
+//    after the PV that reads the P it overwrites, and S_g(i) completes after PV_g(i-1), so
+//    O_g is stable whenever the softmax sees a new S_g. Key tiles past the causal limit of
 //    tile A are not multiplied for A.
 //  * Softmax: 8 warps, thread r of a warpgroup owns row r of its tile (TMEM lane r): scores
-//    are masked by key index (causal and length), reduced with tree max/sum, the running max
-//    is only moved when it grows by more than 2^8 (then O is rescaled in tensor memory), and
-//    P is written as bf16 in the 128-byte-swizzled K-major layout the MMA reads. Rows of the
-//    last V tile past the sequence are zeroed, so stale or poisoned rows never meet a zero
-//    probability.
+//    are masked by key index (causal and length) on boundary tiles only, reduced with tree
+//    max/sum, the running max is only moved when it grows by more than 2^8 (then O is
+//    rescaled in tensor memory), and p = 2^(s*scale - m) comes from one packed fma per pair.
+//    Rows of the last V tile past the sequence are zeroed, so stale or poisoned rows never
+//    meet a zero probability.
 //  * Every wait is bounded; on a timeout the kernel records PA_DEV_ERR_TIMEOUT, runs to
 //    the end of its protocol and frees its tensor memory.
 #include <cuda.h>
@@ -47,31 +50,32 @@ namespace pa {
 namespace {
 
 constexpr int kRows = 128;                 // query rows per tile (TMEM lanes)
-constexpr int kKeys = 64;                  // keys per K/V tile
-constexpr int kStages = 4;                 // K/V ring depth
-constexpr int kQHalf = 128 * 128;          // 128 rows x 64 dims (one swizzled column block)
-constexpr int kKVHalf = kKeys * 128;       // 64 rows x 64 dims
+constexpr int kKeys = 128;                 // keys per K/V tile
+constexpr int kKStages = 3, kVStages = 2;  // ring depths
+constexpr int kHalf = 128 * 128;           // 128 rows x 64 dims: one swizzled column block
+constexpr int kTile = 2 * kHalf;           // 128 x 128 bf16
 constexpr int kThreads = 320;              // warps 0-3 tile A, 4-7 tile B, 8 TMA, 9 MMA
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S of tile g, buffer b at g*128 + b*64; O of tile g at 256 + g*128.
-__host__ __device__ constexpr uint32_t col_s(int g, int b) { return (uint32_t)(g * 128 + b * 64); }
-__host__ __device__ constexpr uint32_t col_o(int g) { return (uint32_t)(256 + g * 128); }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows 256x
+
+// TMEM columns: S (then P) of tile g at g*128, O of tile g at 256 + g*128.
+__host__ __device__ constexpr uint32_t col_s(int g) { return (uint32_t)(g * 128); }
+__host__ __device__ constexpr uint32_t col_o(int g) { return (uint32_t)(256 + g * 128); }
 
 struct PrefillSmem {
   // 1024-byte aligned tiles (128-byte swizzle atoms are 1024 bytes)
-  unsigned char q[2][2 * kQHalf];          // [tile][dim half]
-  unsigned char p[2][kRows * 128];         // [tile] 128 rows x 64 keys
-  unsigned char k[kStages][2 * kKVHalf];   // [stage][dim half]
-  unsigned char v[kStages][2 * kKVHalf];
+  unsigned char q[2][kTile];         // [tile]
+  unsigned char k[kKStages][kTile];  // [stage]
+  unsigned char v[kVStages][kTile];
   uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2][2];                   // [tile][buffer]
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];        // S products of that K stage done
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];        // PV products of that V stage done
+  uint64_t s_full[2];                // [tile]
   uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t o_done[2];                // the tile's last PV done
   uint32_t tmem_base;
   int abort;
 };
@@ -123,14 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&sm.q_full, 2 * kRows);
-    for (int b = 0; b < kStages; ++b) {
+    for (int b = 0; b < kKStages; ++b) {
       mbar_init(&sm.k_full[b], 1);
+      mbar_init(&sm.k_empty[b], 1);
+    }
+    for (int b = 0; b < kVStages; ++b) {
       mbar_init(&sm.v_full[b], 1);
-      mbar_init(&sm.kv_empty[b], 1);
+      mbar_init(&sm.v_empty[b], 1);
     }
     for (int g = 0; g < 2; ++g) {
-      mbar_init(&sm.s_full[g][0], 1);
-      mbar_init(&sm.s_full[g][1], 1);
+      mbar_init(&sm.s_full[g], 1);
       mbar_init(&sm.p_full[g], kRows);
       mbar_init(&sm.o_done[g], 1);
     }
@@ -156,13 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int box_rows = bs < kKeys ? bs : kKeys;
       const int boxes = kKeys / box_rows;
       const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
-      for (int it = 0; it < n_all; ++it) {
-        const int st = it % kStages;
-        if (it >= kStages &&
-            !mbar_wait(&sm.kv_empty[st], (uint32_t)(((it / kStages) - 1) & 1), abort_flag))
+      auto load = [&](bool is_v, int it) {
+        const int stages = is_v ? kVStages : kKStages;
+        const int st = it % stages;
+        uint64_t* empty = is_v ? &sm.v_empty[st] : &sm.k_empty[st];
+        uint64_t* full = is_v ? &sm.v_full[st] : &sm.k_full[st];
+        if (it >= stages && !mbar_wait(empty, (uint32_t)(((it / stages) - 1) & 1), abort_flag))
           note_timeout(sm, a.dev_err);
         const int t0 = it * kKeys;
-        int blk[kKeys / 8];  // at most 8 boxes (block_size 8)
+        int blk[kKeys / 8];  // at most 16 boxes (block_size 8)
         uint32_t bytes = 0;
         for (int bx = 0; bx < boxes; ++bx) {
           const int key0 = t0 + bx * box_rows;
@@ -172,26 +180,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (id >= 0 && (int64_t)id < a.num_blocks) {
               blk[bx] = id;
               bytes += 2u * box_rows * 128u;
-            } else {
+            } else if (!is_v) {
               set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
             }
           }
         }
         const int row0 = (bs > kKeys) ? (t0 % bs) : 0;
-        mbar_arrive_expect_tx(&sm.k_full[st], bytes);
+        unsigned char* dst = is_v ? sm.v[st] : sm.k[st];
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+        mbar_arrive_expect_tx(full, bytes);
         for (int bx = 0; bx < boxes; ++bx) {
           if (blk[bx] < 0) continue;
           for (int h2 = 0; h2 < 2; ++h2)
-            umma::tma_load_4d(sm.k[st] + h2 * kKVHalf + bx * box_rows * 128, &tm_k, h2 * 64, j,
-                              row0, blk[bx], &sm.k_full[st]);
+            umma::tma_load_4d(dst + h2 * kHalf + bx * box_rows * 128, map, h2 * 64, j, row0,
+                              blk[bx], full);
         }
-        mbar_arrive_expect_tx(&sm.v_full[st], bytes);
-        for (int bx = 0; bx < boxes; ++bx) {
-          if (blk[bx] < 0) continue;
-          for (int h2 = 0; h2 < 2; ++h2)
-            umma::tma_load_4d(sm.v[st] + h2 * kKVHalf + bx * box_rows * 128, &tm_v, h2 * 64, j,
-                              row0, blk[bx], &sm.v_full[st]);
-        }
+      };
+      // K runs one tile ahead of V: S(i+1) is issued right after PV(i)
+      load(false, 0);
+      for (int it = 0; it < n_all; ++it) {
+        load(true, it);
+        if (it + 1 < n_all) load(false, it + 1);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -199,60 +208,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma::idesc_bf16_f32(kRows, kKeys, false);
       constexpr uint32_t idesc_o = umma::idesc_bf16_f32(kRows, 128, true);
+      auto issue_s = [&](int g, int it) {  // S_g = Q_g K(it)^T
+        const uint32_t k_addr = smem_u32(sm.k[it % kKStages]);
+        const uint32_t q_addr = smem_u32(sm.q[g]);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma::mma_bf16(tmem + col_s(g), umma::smem_desc(q_addr + off, 16, 1024),
+                         umma::smem_desc(k_addr + off, 16, 1024), idesc_s, kk > 0);
+        }
+        umma::commit(&sm.s_full[g]);
+      };
+      auto issue_pv = [&](int g, int it) {  // O_g += P_g V(it), P_g read from tensor memory
+        const uint32_t v_addr = smem_u32(sm.v[it % kVStages]);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma::mma_bf16_ts(tmem + col_o(g), tmem + col_s(g) + kk * 8,
+                            umma::smem_desc(v_addr + kk * 16 * 128, kHalf, 1024), idesc_o,
+                            (it > 0) || (kk > 0));
+        if (it == n_tiles[g] - 1) umma::commit(&sm.o_done[g]);
+      };
+      auto wait_k = [&](int it) {
+        if (!mbar_wait(&sm.k_full[it % kKStages], (uint32_t)((it / kKStages) & 1), abort_flag))
+          note_timeout(sm, a.dev_err);
+        umma::fence_after_sync();
+      };
       if (!mbar_wait(&sm.q_full, 0, abort_flag)) note_timeout(sm, a.dev_err);
       umma::fence_after_sync();
-      auto issue_pv = [&](int it) {
-        const int st = it % kStages;
-        const uint32_t v_addr = smem_u32(sm.v[st]);
-        bool v_ready = false;
+      wait_k(0);
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (n_tiles[g] > 0) issue_s(g, 0);
+      umma::commit(&sm.k_empty[0]);
+      for (int it = 0; it < n_all; ++it) {
+        bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           if (it >= n_tiles[g]) continue;
           if (!mbar_wait(&sm.p_full[g], (uint32_t)(it & 1), abort_flag)) note_timeout(sm, a.dev_err);
           if (!v_ready) {
-            if (!mbar_wait(&sm.v_full[st], (uint32_t)((it / kStages) & 1), abort_flag))
+            if (!mbar_wait(&sm.v_full[it % kVStages], (uint32_t)((it / kVStages) & 1), abort_flag))
               note_timeout(sm, a.dev_err);
             v_ready = true;
           }
           umma::fence_after_sync();
-          const uint32_t p_addr = smem_u32(sm.p[g]);
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t ad = umma::smem_desc(p_addr + kk * 32, 16, 1024);
-            const uint64_t bd = umma::smem_desc(v_addr + kk * 16 * 128, kKVHalf, 1024);
-            umma::mma_bf16(tmem + col_o(g), ad, bd, idesc_o, (it > 0) || (kk > 0));
+          issue_pv(g, it);
+          if (it + 1 < n_tiles[g]) {
+            if (!k_ready) {
+              wait_k(it + 1);
+              k_ready = true;
+            }
+            issue_s(g, it + 1);
           }
-          umma::commit(&sm.o_done[g]);
         }
-        umma::commit(&sm.kv_empty[st]);
-      };
-      for (int it = 0; it < n_all; ++it) {
-        const int st = it % kStages;
-        if (!mbar_wait(&sm.k_full[st], (uint32_t)((it / kStages) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
-        umma::fence_after_sync();
-        const uint32_t k_addr = smem_u32(sm.k[st]);
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          if (it >= n_tiles[g]) continue;
-          const uint32_t q_addr = smem_u32(sm.q[g]);
-#pragma unroll
-          for (int kk = 0; kk < 128 / 16; ++kk) {
-            const uint64_t ad = umma::smem_desc(q_addr + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = umma::smem_desc(k_addr + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024);
-            umma::mma_bf16(tmem + col_s(g, it & 1), ad, bd, idesc_s, kk > 0);
-          }
-          umma::commit(&sm.s_full[g][it & 1]);
-        }
-        if (it > 0) issue_pv(it - 1);
+        umma::commit(&sm.v_empty[it % kVStages]);
+        if (k_ready) umma::commit(&sm.k_empty[(it + 1) % kKStages]);
       }
-      issue_pv(n_all - 1);
       // the last products must land before tensor memory is released
 #pragma unroll
       for (int g = 0; g < 2; ++g)
-        if (n_tiles[g] > 0 &&
-            !mbar_wait(&sm.o_done[g], (uint32_t)((n_tiles[g] - 1) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
+        if (n_tiles[g] > 0 && !mbar_wait(&sm.o_done[g], 0, abort_flag)) note_timeout(sm, a.dev_err);
     }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
@@ -276,21 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ch = 0; ch < 16; ++ch) qv[ch] = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch)
-        *reinterpret_cast<uint4*>(sm.q[g] + (ch >> 3) * kQHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(sm.q[g] + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
             qv[ch];
       fence_proxy_async_smem();
       mbar_arrive(&sm.q_full);
     }
 
     float m_run = -INFINITY, l_run = 0.f;
+    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
     for (int it = 0; it < nt; ++it) {
-      const int buf = it & 1;
-      if (!mbar_wait(&sm.s_full[g][buf], (uint32_t)((it >> 1) & 1), abort_flag))
-        note_timeout(sm, a.dev_err);
+      if (!mbar_wait(&sm.s_full[g], (uint32_t)(it & 1), abort_flag)) note_timeout(sm, a.dev_err);
       umma::fence_after_sync();
       float sv[kKeys];
-      umma::tmem_ld32(lane_addr + col_s(g, buf), sv);
-      umma::tmem_ld32(lane_addr + col_s(g, buf) + 32, sv + 32);
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) umma::tmem_ld32(lane_addr + col_s(g) + 32 * c4, sv + 32 * c4);
       umma::tmem_ld_wait();
 
       const int t0 = it * kKeys;
@@ -322,8 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = 1.f;
       }
       const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
-      // p = 2^(s*scale - m): one packed fma per pair of scores, then ex2
-      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      // p = 2^(s*scale - m): one packed fma per pair, then ex2; P packed as bf16 pairs over S
       const float2 nm2 = make_float2(-m_safe, -m_safe);
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
@@ -331,22 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kKeys / 2; ++c) {
         const float2 x = umma::ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sc2, nm2);
         const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        sv[2 * c] = p.x;
-        sv[2 * c + 1] = p.y;
         acc[c & 3] = umma::fadd2(acc[c & 3], p);
+        sv[c] = __uint_as_float(f32x2_to_bf16x2(p.x, p.y));  // c <= 2c: in place is safe
       }
       const float2 t01 = umma::fadd2(acc[0], acc[1]), t23 = umma::fadd2(acc[2], acc[3]);
       const float2 tt = umma::fadd2(t01, t23);
-      const float rs = tt.x + tt.y;
-      l_run = l_run * alpha + rs;
+      l_run = l_run * alpha + (tt.x + tt.y);
       m_run = m_use;
-
-      // O and the P buffer of this tile belong to PV(it-1) until it completes
-      if (it > 0) {
-        if (!mbar_wait(&sm.o_done[g], (uint32_t)((it - 1) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
-        umma::fence_after_sync();
-      }
+      umma::tmem_st32(lane_addr + col_s(g), sv);
+      umma::tmem_st32(lane_addr + col_s(g) + 32, sv + 32);
+      // O_g is stable here (S_g(it) completed after PV_g(it-1)); PV_g(it) waits for p_full
       if (__any_sync(0xffffffffu, rescale)) {
         float ob[32];
 #pragma unroll
@@ -357,40 +364,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e) ob[e] *= alpha;
           umma::tmem_st32(lane_addr + col_o(g) + 32 * c4, ob);
         }
-        umma::tmem_st_wait();
       }
       // rows of the last V tile beyond the sequence: zero them (never multiply a stale row)
       if (t0 + kKeys > kv_len) {
-        const int st = it % kStages;
-        if (!mbar_wait(&sm.v_full[st], (uint32_t)((it / kStages) & 1), abort_flag))
+        const int st = it % kVStages;
+        if (!mbar_wait(&sm.v_full[st], (uint32_t)((it / kVStages) & 1), abort_flag))
           note_timeout(sm, a.dev_err);
         const int first_bad = kv_len - t0;
-        for (int idx = r; idx < kKeys * 16; idx += kRows) {
-          const int row = idx >> 4, ch = idx & 15;
-          if (row >= first_bad)
-            *reinterpret_cast<uint4*>(sm.v[st] + (ch >> 3) * kKVHalf + row * 128 + (ch & 7) * 16) =
+        if (r >= first_bad) {
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch)
+            *reinterpret_cast<uint4*>(sm.v[st] + (ch >> 3) * kHalf + r * 128 + (ch & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();
       }
-      // P row (bf16) -> shared memory, 128-byte swizzled K-major (64 keys = one 128 B row)
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 pk;
-        pk.x = f32x2_to_bf16x2(sv[8 * ch + 0], sv[8 * ch + 1]);
-        pk.y = f32x2_to_bf16x2(sv[8 * ch + 2], sv[8 * ch + 3]);
-        pk.z = f32x2_to_bf16x2(sv[8 * ch + 4], sv[8 * ch + 5]);
-        pk.w = f32x2_to_bf16x2(sv[8 * ch + 6], sv[8 * ch + 7]);
-        *reinterpret_cast<uint4*>(sm.p[g] + r * 128 + ((ch ^ (r & 7)) << 4)) = pk;
-      }
-      fence_proxy_async_smem();
+      umma::tmem_st_wait();
       umma::fence_before_sync();
       mbar_arrive(&sm.p_full[g]);
     }
 
     // ---- epilogue: O / l -> bf16 rows ------------------------------------------------
     if (nt > 0) {
-      if (!mbar_wait(&sm.o_done[g], (uint32_t)((nt - 1) & 1), abort_flag))
-        note_timeout(sm, a.dev_err);
+      if (!mbar_wait(&sm.o_done[g], 0, abort_flag)) note_timeout(sm, a.dev_err);
       umma::fence_after_sync();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
