@@ -47,14 +47,26 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_traffic(kernel_src: str, summary: str):
+def source_sha256(*names) -> str:
+    """sha256 over the named csrc/ files, in order (the kernel and the headers it uses)."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_107_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+DECODE_SOURCES = ("decode.cu", "pa_device.cuh")
+PREFILL_SOURCES = ("prefill.cu", "umma.cuh", "pa_device.cuh")
+
+
+def kernel_traffic(sources, summary: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
-    kernel source (sha256 recorded in the summary); otherwise None."""
+    kernel sources (sha256 recorded in the summary); otherwise None."""
     path = os.path.join(ROOT, "profiles", summary)
-    src = os.path.join(ROOT, "paged_kv_cache_107_gb300", "csrc", kernel_src)
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = source_sha256(*sources)
         m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
         m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
         if m_sha and m_b and m_sha.group(1) == sha:
@@ -430,7 +442,7 @@ def run_ours(args):
     hbm_peak, _, peak_src = measured_peaks()
     decode_alg_bytes = kv_bytes + small_bytes
     achieved = decode_alg_bytes / (decode_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("decode.cu", "decode_w2_qwen3_b256.md")
+    traffic = kernel_traffic(DECODE_SOURCES, "decode_w2_qwen3_b256.md")
 
     # ---- end to end through the public API with host buffers ---------------------------
     pin = lambda t: t.pin_memory()
