@@ -1,0 +1,79 @@
+"""The decode step as the engine runs it ("3.6 ModelRunner、CUDA Graph 与性能基准",
+section 5): store + decode captured once in a CUDA graph for a batch-size bucket, then
+replayed with new inputs copied into static buffers; rows past the real batch are
+padding (slot_mapping = -1, context_lens = 0). Every replay must match the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_107_gb300 as pk
+from paged_kv_cache_107_gb300 import workloads
+from tests.gpu_helpers import assert_close, bits, from_bits, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_step_graph_replay_with_padding_rows():
+    dev = torch.device("cuda")
+    bucket, H, Hk, D, bs = 16, 16, 8, 128, 16
+    maxb = 40
+    nb = 2048
+    base = workloads.decode_case([1] * bucket, H, Hk, D, bs, num_blocks=nb, seed=107900,
+                                 max_blocks=maxb)
+    kc = base.k_cache.to(dev)
+    vc = base.v_cache.to(dev)
+    # static graph inputs (the bucket's buffers)
+    q = torch.zeros((bucket, H, D), dtype=torch.bfloat16, device=dev)
+    k_new = torch.zeros((bucket, Hk, D), dtype=torch.bfloat16, device=dev)
+    v_new = torch.zeros_like(k_new)
+    slots = torch.full((bucket,), -1, dtype=torch.int32, device=dev)
+    ctx = torch.zeros((bucket,), dtype=torch.int32, device=dev)
+    bt = torch.full((bucket, maxb), -1, dtype=torch.int32, device=dev)
+    out = torch.zeros((bucket, H, D), dtype=torch.bfloat16, device=dev)
+    ws = pk.DecodeWorkspace(bucket, H, Hk, D, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        pk.pa_store_kvcache(k_new, v_new, kc, vc, slots, dev_err=err)
+        pk.pa_decode(out, q, kc, vc, bt, ctx, workspace=ws, dev_err=err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    rng = np.random.default_rng(107901)
+    for real in (16, 11, 3, 1):
+        # a fresh batch of `real` sequences over the same pool; the rest are padding rows
+        lens = rng.integers(1, maxb * bs, size=real)
+        case = workloads.decode_case(lens, H, Hk, D, bs, num_blocks=nb,
+                                     seed=int(rng.integers(1 << 30)), max_blocks=maxb)
+        kc.copy_(case.k_cache.to(dev))
+        vc.copy_(case.v_cache.to(dev))
+        q.zero_()
+        q[:real] = case.q.to(dev)
+        k_new[:real] = case.k_new.to(dev)
+        v_new[:real] = case.v_new.to(dev)
+        slots.fill_(-1)
+        slots[:real] = torch.from_numpy(case.slot_mapping).to(dev)
+        ctx.zero_()
+        ctx[:real] = torch.from_numpy(case.context_lens).to(dev)
+        bt.fill_(-1)
+        bt[:real] = torch.from_numpy(case.block_tables).to(dev)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ok, ov = oracle.store_kvcache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                      case.slot_mapping)
+        assert np.array_equal(bits(kc), ok) and np.array_equal(bits(vc), ov)
+        ref = oracle.decode(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+                            case.context_lens)
+        got = to_f64(out)
+        assert_close(got[:real], ref, f"replay with {real} real rows")
+        assert np.all(got[real:] == 0.0), "padding rows must be zero"
