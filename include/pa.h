@@ -122,11 +122,14 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *   grid_ctas       number of CTAs that split the key stream (0 = one per SM). The result
  *                   does not depend on it beyond fp32 rounding of the final combine.
  *   workspace       device scratch of at least pa_decode_workspace_size(...) bytes,
- *                   256-byte aligned. Its first num_seqs*num_kv_heads int32 words are
- *                   arrival counters that must be ZERO before the first call; every
- *                   successful call leaves them zero again (after a PA_DEV_ERR_TIMEOUT
- *                   the caller must zero them). Calls that overlap in time must use
- *                   different workspaces.
+ *                   256-byte aligned; zero it once when it is created. It holds the
+ *                   partial results, then num_seqs*num_kv_heads int32 arrival counters
+ *                   that must be zero before a call; every successful call leaves them
+ *                   zero again (after a PA_DEV_ERR_TIMEOUT the caller must zero the
+ *                   workspace). The counters' offset depends only on the device and
+ *                   num_heads, so a workspace sized for B sequences serves any call
+ *                   with num_seqs <= B and the same num_heads / num_kv_heads. Calls that
+ *                   overlap in time must use different workspaces.
  *
  * Arithmetic: bf16 inputs, fp32 products, fp32 online softmax and accumulation, one
  * bf16 round-to-nearest-even at the end.
@@ -136,6 +139,49 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
               int64_t num_blocks, float scale, int grid_ctas, void* workspace,
               size_t workspace_bytes, int* dev_err, void* stream);
+
+/*
+ * pa_decode_step — one decode step of the path in ONE launch: the store of every
+ * sequence's new token followed by the decode over the cache that includes it.
+ * Source: "nano-vllm解读", sections "KVCache的写入" (each layer first writes the new K/V at
+ * slot_mapping, then attends) and "CUDAGraph优化" (the decode step is replayed from a
+ * captured graph per batch bucket; padding rows carry slot -1 and context length 0);
+ * "3.6 ModelRunner…", section 2 (the decode token of sequence b is stored at the slot of
+ * its last position, context_lens[b] = len(seq)) and section 5 (graph buckets
+ * 1, 2, 4, 8, 16, 32, …, padded with slot -1 / context 0).
+ *
+ * Same result, bit for bit, as pa_store_kvcache(k_new, v_new, ..., slot_mapping,
+ * num_tokens = num_seqs) followed by pa_decode(...) with the other arguments, for every
+ * input where each slot_mapping[b] is -1 or the slot of position context_lens[b]-1 of
+ * sequence b (block_tables[b][p/bs]*bs + p%bs, p = context_lens[b]-1), which is how the
+ * decode step builds it.
+ *
+ *   k_new, v_new    device, bf16; row b (start k_new + b*k_new_stride elements) holds
+ *                   the num_kv_heads*head_dim values of sequence b's new token.
+ *   k_new_stride,
+ *   v_new_stride    token strides in ELEMENTS, >= num_kv_heads*head_dim and multiples of 8
+ *                   (k_new, v_new 16-byte aligned), else PA_ERR_ALIGN.
+ *   k_cache,v_cache written at the new tokens' slots, read everywhere else.
+ *   slot_mapping    device, int32 [num_seqs]. -1: nothing is stored and the cache row at
+ *                   position context_lens[b]-1 is read as it is. Any other value that is
+ *                   not the slot of that position (or a token of a sequence with context
+ *                   length 0) sets PA_DEV_ERR_SLOT and that token is NOT stored (another
+ *                   sequence of the same launch might be reading that row).
+ *   everything else as pa_decode (same workspace rules; one workspace per call in flight).
+ *
+ * The store and the attention share one read of each new row: the CTA that owns a
+ * sequence's last key tile copies that row from k_new/v_new into its tile and writes it to
+ * the cache. Rows of other sequences that alias the new token's slot (never the case when
+ * the slot's block holds the newest position of only one sequence) race with the store.
+ * Graph-capturable: no host synchronisation, no allocation, fixed grid for any batch.
+ */
+int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
+                   int64_t k_new_stride, int64_t v_new_stride, void* k_cache, void* v_cache,
+                   const int32_t* slot_mapping, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                   int num_heads, int num_kv_heads, int head_dim, int block_size,
+                   int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+                   size_t workspace_bytes, int* dev_err, void* stream);
 
 /*
  * pa_decode_noalloc — pa_decode for callers that cannot allocate device memory.

@@ -18,7 +18,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["pa_store_kvcache", "pa_decode", "pa_decode_workspace_size", "pa_prefill_varlen",
+__all__ = ["pa_store_kvcache", "pa_decode", "pa_decode_step", "pa_decode_workspace_size",
+           "pa_prefill_varlen", "pa_decode_noalloc",
            "pa_status_str", "pa_version", "DecodeWorkspace", "library_path", "load_library",
            "PA_DEV_ERR"]
 
@@ -62,6 +63,9 @@ def load_library(path: Optional[str] = None):
         lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32,
                                   i32, vp, sz, vp, vp]
         lib.pa_decode.restype = i32
+        lib.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, i32, vp, i32,
+                                       i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp]
+        lib.pa_decode_step.restype = i32
         lib.pa_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                           i32, i32, i64, i32, f32, vp, vp]
         lib.pa_prefill_varlen.restype = i32
@@ -191,6 +195,48 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
         float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(workspace.buffer),
         workspace.nbytes, _ptr(dev_err), _stream(stream))
     _check(rc, "pa_decode")
+    return out
+
+
+def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                   block_tables: torch.Tensor, context_lens: torch.Tensor,
+                   scale: Optional[float] = None, grid_ctas: int = 0,
+                   workspace: Optional[DecodeWorkspace] = None,
+                   dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Store of each sequence's new token plus decode, in one launch: the same result as
+    pa_store_kvcache(k_new, v_new, ..., slot_mapping) then pa_decode(...). k_new, v_new
+    [B, Hk, D] bf16 (token stride a multiple of 8 elements); slot_mapping [B] int32, -1 or
+    the slot of position context_lens[b]-1 of sequence b."""
+    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
+                            ("k_cache", k_cache, torch.bfloat16, 4),
+                            ("v_cache", v_cache, torch.bfloat16, 4),
+                            ("block_tables", block_tables, torch.int32, 2),
+                            ("context_lens", context_lens, torch.int32, 1),
+                            ("slot_mapping", slot_mapping, torch.int32, 1)):
+        _need(t, name, dt, nd)
+        if not t.is_contiguous():
+            raise PagedAttentionError(f"{name} must be contiguous")
+    _need(k_new, "k_new", torch.bfloat16, 3)
+    _need(v_new, "v_new", torch.bfloat16, 3)
+    B, H, D = q.shape
+    nb, bs, hk, d2 = k_cache.shape
+    if out.shape != q.shape or d2 != D or v_cache.shape != k_cache.shape:
+        raise PagedAttentionError("shape mismatch")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B or slot_mapping.shape[0] != B:
+        raise PagedAttentionError("block_tables / context_lens / slot_mapping batch mismatch")
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t.shape != (B, hk, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise PagedAttentionError(f"{name} must be [B, Hk, D] with contiguous rows")
+    if workspace is None:
+        workspace = _default_workspace(B, H, hk, D, q.device)
+    rc = load_library().pa_decode_step(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0), v_new.stride(0),
+        _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, H, hk, D, bs, nb,
+        float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(workspace.buffer),
+        workspace.nbytes, _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_decode_step")
     return out
 
 

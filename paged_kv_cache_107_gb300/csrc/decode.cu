@@ -1,809 +1,8 @@
-// decode.cu — paged GQA decode attention on CUDA cores (bandwidth-bound GEMV).
-//
-// What it computes ("nano-vllm解读", sections "PageAttention原理" and "Nano-vllm中的使用";
-// "3.6 ModelRunner、CUDA Graph 与性能基准", section 2): for every sequence b and query head
-// h, o = softmax(scale * q_h K^T) V over the first context_lens[b] cached tokens of KV
-// head h / (H/H_kv), where token t lives at row block_tables[b][t / bs] * bs + t % bs.
-// The softmax is evaluated online, tile by tile, as the FlashAttention description on the
-// nano-vllm overview page ("FlashAttention 核心思想") lays out: load a K/V tile into on-chip
-// memory, update the running max and sum, accumulate, discard the tile.
-//
-// GB300 design
-//  * Work split ("stream-K" over key tiles). Every sequence is cut into tiles of T tokens;
-//    all tiles of all sequences form one stream of NT tiles, and CTA c of the grid takes
-//    tiles [c*NT/G, (c+1)*NT/G). Every CTA therefore reads the same number of bytes
-//    whatever the length mix. A sequence whose tiles all fall in one CTA is written
-//    directly; a sequence cut between CTAs leaves one partial (o, log-sum-exp) per CTA,
-//    and the last CTA to finish it (arrival counter) combines them in CTA order, so the
-//    result is deterministic.
-//  * One CTA handles a slab of HS KV heads (all of them when H_kv <= 8), so one token's
-//    rows for the slab are HS*256 contiguous bytes: the producer warp moves each token row
-//    with one cp.async.bulk (TMA engine) into a STAGES-deep shared-memory ring guarded by
-//    mbarriers. Tiles never need block alignment: each token's row is addressed through
-//    the block table on its own.
-//  * 8 consumer warps (+1 producer warp: 9 warps keep 168 registers per thread):
-//    warp (j, w) owns KV head j of the slab and 16 tokens of every tile; a half-warp
-//    holds one token row (16 lanes x 16 bytes), so each K row is read from shared memory
-//    once and reused for all G = H/H_kv query heads of the group. Partial
-//    dot products are reduced with a butterfly that halves the value count at every
-//    shuffle stage (about one shuffle per score). fp32 online softmax with exp2 on
-//    pre-scaled q; fp32 accumulation; one bf16 rounding at the end.
-#include <cuda_runtime.h>
-#include <math.h>
-#include <stdint.h>
-
-#include "pa_device.cuh"
-#include "pa_launch.h"
+// decode.cu — host side of pa_decode: workspace layout, head-slab choice and the
+// launch of the decode kernel (decode_kernel.cuh) without the fused store.
+#include "decode_kernel.cuh"
 
 namespace pa {
-namespace {
-
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kTokPerWarp = 16;
-constexpr int kPairs = kTokPerWarp / 2;  // token pairs (one per half-warp) per warp and tile
-constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagWhole = 4;
-
-template <int HS, int G>
-struct DecCfg {
-  static constexpr int T = 128 / HS;                // tokens per stage
-  static constexpr int WPH = kConsumerWarps / HS;   // consumer warps per KV head
-  static constexpr int ROW = HS * kHeadDim * 2;     // bytes of one token row of the slab
-  static constexpr int KV_BYTES = T * ROW;          // K (or V) bytes per stage
-  static constexpr int Q_BYTES = HS * G * kHeadDim * 2;
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int STAGES = (3 * STAGE_BYTES + 8192 <= 227 * 1024) ? 3 : 2;
-  static constexpr int NV = kPairs * G;             // partial scores per lane per tile
-  static constexpr int CF = NV >= 16 ? NV / 16 : 1;  // scores per lane after the reduction
-  static constexpr int MERGE_FLOATS = G * (kHeadDim + 2);
-  static constexpr int PBUF_FLOATS = 2 * kPairs * G;  // per warp: [half][pair][head]
-  static constexpr int CTRL_BYTES = 4096 + kConsumerWarps * PBUF_FLOATS * 4;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + CTRL_BYTES + 128;
-  static_assert(T == WPH * kTokPerWarp, "tile / warp split");
-  static_assert((kConsumerWarps - HS) * MERGE_FLOATS * 4 <= 2 * KV_BYTES, "merge scratch");
-};
-
-struct __align__(16) StageMeta {
-  int64_t pb;     // first tile of the sequence in the global tile stream
-  int b;          // sequence
-  int tok0;       // first token of the tile
-  int count;      // valid tokens in the tile
-  int nb;         // tiles of the sequence
-  int flags;
-  int pad;
-};
-
-struct Ctrl {
-  uint64_t full[3];
-  uint64_t empty[3];
-  uint64_t seg_bar;
-  uint64_t merge_bar[8];
-  StageMeta meta[3];
-  int64_t nt;      // tiles in the stream
-  int64_t x0, x1;  // this CTA's tile range
-  int64_t pb0;     // first tile of the sequence holding x0
-  int b0;
-  int g_eff;       // CTAs that own tiles
-  int found;
-  int abort;
-  int64_t red[32];
-};
-
-__device__ __forceinline__ int load_ctx(const int32_t* ctx, int b, int cap) {
-  const int n = __ldg(ctx + b);
-  return (n < 0 || n > cap) ? 0 : n;
-}
-
-// CTA of the balanced split that owns tile x: the largest c with floor(c*NT/G) <= x.
-__device__ __forceinline__ int64_t cta_of(int64_t x, int64_t nt, int g) {
-  return ((x + 1) * g - 1) / nt;
-}
-__device__ __forceinline__ int64_t tile_begin(int64_t c, int64_t nt, int g) {
-  return (c * nt) / g;
-}
-
-// One butterfly stage over the 16 lanes of a half-warp: N values -> N/2 values, or a plain
-// all-reduce once a single value is left.
-template <int N>
-__device__ __forceinline__ void bfly(float* v, int sub, int mask) {
-  if constexpr (N > 1) {
-    const bool up = (sub & mask) != 0;
-#pragma unroll
-    for (int k = 0; k < N / 2; ++k) {
-      const float send = up ? v[k] : v[k + N / 2];
-      const float keep = up ? v[k + N / 2] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-    }
-  } else {
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
-  }
-}
-
-template <int N>
-struct Half {
-  static constexpr int v = N > 1 ? N / 2 : 1;
-};
-
-// After the butterfly, lane value r holds flattened index kb + r, kb from the lane bits.
-template <int NV>
-__device__ __forceinline__ int bfly_base(int sub) {
-  int kb = 0, c = NV;
-#pragma unroll
-  for (int m = 8; m >= 1; m >>= 1) {
-    if (c > 1) {
-      c >>= 1;
-      if (sub & m) kb += c;
-    }
-  }
-  return kb;
-}
-
-// Value for head hh taken from the lane that owns it. After the butterfly the flattened
-// index is kk = pair*G + hh, the pair bits sit in sub-lane bits 3..1 and the head in
-// sub-lane bit 0 and the value index r: hh = (sub & 1) * CF + r.
-template <int G, int CF>
-__device__ __forceinline__ float head_bcast(const float* vals, int hh, int lane) {
-  if constexpr (G == 1) {
-    return vals[0];
-  } else {
-    // hh is a compile-time constant at every (unrolled) call site
-    return __shfl_sync(0xffffffffu, vals[hh % CF], (lane & ~1) | (hh / CF));
-  }
-}
-
-// Packed fp32x2 arithmetic (two independent fp32 lanes per instruction).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
-        "l"(*reinterpret_cast<const uint64_t*>(&c)));
-  return *reinterpret_cast<const float2*>(&d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
-  return *reinterpret_cast<const float2*>(&d);
-}
-// Two bf16 (element 0 in the low half) widened to an fp32 pair.
-__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-template <int HS, int G>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_decode_kernel(const DecodeArgs a) {
-  using C = DecCfg<HS, G>;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + (size_t)C::STAGES * C::STAGE_BYTES);
-  float* pbuf_all = reinterpret_cast<float*>(smem + (size_t)C::STAGES * C::STAGE_BYTES + 4096);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int c = blockIdx.x;
-  const int slab = blockIdx.y;
-  const int H = a.num_heads;
-  const int Hk = a.num_kv_heads;
-  const int cap = a.max_blocks * a.block_size;
-  const int B = a.num_seqs;
-  constexpr int T = C::T;
-
-  if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&ctl.full[s], 1);
-      mbar_init(&ctl.empty[s], kConsumerWarps);
-    }
-    mbar_init(&ctl.seg_bar, kConsumerWarps);
-    if (C::WPH > 1)
-      for (int j = 0; j < HS; ++j) mbar_init(&ctl.merge_bar[j], C::WPH - 1);
-    ctl.found = 0;
-    ctl.abort = 0;
-    ctl.b0 = 0;
-    ctl.pb0 = 0;
-    fence_mbar_init();
-  }
-
-  // ---- prologue: total tiles, then the sequence that holds this CTA's first tile -----
-  int64_t local = 0;
-  for (int b = tid; b < B; b += kThreads) {
-    const int raw = __ldg(a.context_lens + b);
-    if (raw < 0 || raw > cap) {
-      if ((b % gridDim.x) == c && slab == 0) set_dev_err(a.dev_err, PA_DEV_ERR_CONTEXT);
-    }
-    local += (load_ctx(a.context_lens, b, cap) + T - 1) / T;
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) local += __shfl_xor_sync(0xffffffffu, local, m);
-  if (lane == 0) ctl.red[warp] = local;
-  __syncthreads();
-  if (tid == 0) {
-    int64_t nt = 0;
-    for (int w = 0; w < kThreads / 32; ++w) nt += ctl.red[w];
-    ctl.nt = nt;
-    const int g_eff = (int)(nt < (int64_t)gridDim.x ? nt : (int64_t)gridDim.x);
-    ctl.g_eff = g_eff;
-    if (c < g_eff) {
-      ctl.x0 = tile_begin(c, nt, g_eff);
-      ctl.x1 = tile_begin(c + 1, nt, g_eff);
-    } else {
-      ctl.x0 = ctl.x1 = 0;
-    }
-  }
-  __syncthreads();
-  const int64_t NT = ctl.nt;
-  const int g_eff = ctl.g_eff;
-  const int64_t x0 = ctl.x0, x1 = ctl.x1;
-
-  // zero rows of empty (or invalid) sequences assigned to this CTA: one warp per row
-  {
-    const int heads_per_slab = HS * G;
-    for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
-      if (load_ctx(a.context_lens, b, cap) != 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                            ((int64_t)b * H + slab * heads_per_slab) * kHeadDim);
-      const int nvec = heads_per_slab * kHeadDim / 8;
-      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
-
-  if (x0 < x1) {
-    // chunked scan over the sequences until the one holding tile x0 is found
-    int64_t running = 0;
-    for (int base = 0; base < B; base += kConsumerWarps * 32) {
-      int n = 0;
-      const int b = base + tid;
-      if (tid < kConsumerWarps * 32 && b < B) n = (load_ctx(a.context_lens, b, cap) + T - 1) / T;
-      int incl = n;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, m);
-        if (lane >= m) incl += y;
-      }
-      if (lane == 31) ctl.red[warp] = incl;
-      __syncthreads();
-      int64_t warp_off = 0;
-      int64_t chunk_total = 0;
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        if (w < warp) warp_off += ctl.red[w];
-        chunk_total += ctl.red[w];
-      }
-      if (tid < kConsumerWarps * 32 && b < B && n > 0) {
-        const int64_t p = running + warp_off + incl - n;
-        if (p <= x0 && x0 < p + n) {
-          ctl.b0 = b;
-          ctl.pb0 = p;
-          ctl.found = 1;
-        }
-      }
-      running += chunk_total;
-      __syncthreads();
-      if (ctl.found) break;
-    }
-  }
-  __syncthreads();
-  // no tiles (all barriers idle; nothing in flight); a start that cannot be located means
-  // context_lens changed under the kernel: flag it and do nothing
-  if (x0 >= x1) return;
-  if (!ctl.found) {
-    if (tid == 0) set_dev_err(a.dev_err, PA_DEV_ERR_CONTEXT);
-    return;
-  }
-
-  const int64_t n_tiles = x1 - x0;
-  volatile int* abort_flag = &ctl.abort;
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ producer
-    const uint64_t policy = policy_evict_first();
-    const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
-    const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
-    const int64_t row_elems = (int64_t)Hk * kHeadDim;
-    const int64_t slab_off = (int64_t)slab * HS * kHeadDim;
-    int b = ctl.b0;
-    int64_t pb = ctl.pb0;
-    int ctx_b = load_ctx(a.context_lens, b, cap);
-    int nb = (ctx_b + T - 1) / T;
-    constexpr int ROWS_PER_LANE = (2 * T + 31) / 32;
-    for (int64_t it = 0; it < n_tiles; ++it) {
-      const int64_t x = x0 + it;
-      while (x >= pb + nb && b + 1 < B) {
-        pb += nb;
-        ++b;
-        ctx_b = load_ctx(a.context_lens, b, cap);
-        nb = (ctx_b + T - 1) / T;
-      }
-      const int s = (int)(it % C::STAGES);
-      const int lt = (int)(x - pb);
-      const int tok0 = lt * T;
-      const int count = min(T, ctx_b - tok0);  // <= 0 only if context_lens changed mid-run
-      int flags = 0;
-      if (x == x0 || lt == 0) flags |= kFlagFirst;
-      if (x == x1 - 1 || lt == nb - 1) flags |= kFlagLast;
-      if (pb >= x0 && pb + nb <= x1) flags |= kFlagWhole;
-
-      // The rows of a tile are one contiguous run when the slab is every KV head and the
-      // tile sits inside one block: then lane 0 moves K and V with one copy each.
-      const int pos_first = tok0, pos_last = tok0 + count - 1;
-      const bool one_run = slab_off == 0 && row_elems == (int64_t)HS * kHeadDim &&
-                           count > 0 && (pos_first / a.block_size) == (pos_last / a.block_size);
-      const uint16_t* src[ROWS_PER_LANE];
-      int ok_rows = 0;
-      if (one_run) {
-#pragma unroll
-        for (int k = 0; k < ROWS_PER_LANE; ++k) src[k] = nullptr;
-        const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos_first / a.block_size);
-        if (blk >= 0 && (int64_t)blk < a.num_blocks) {
-          const int64_t rowi = (int64_t)blk * a.block_size + pos_first % a.block_size;
-          if (lane < 2) {
-            src[0] = (lane ? vc : kc) + rowi * row_elems;
-            ok_rows = count;
-          }
-        } else if (lane == 0) {
-          set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
-        }
-      } else {
-#pragma unroll
-      for (int k = 0; k < ROWS_PER_LANE; ++k) {
-        src[k] = nullptr;
-        const int r = lane + 32 * k;
-        if (r < 2 * T) {
-          const int kv = r >= T;
-          const int t = kv ? r - T : r;
-          if (t < count) {
-            const int pos = tok0 + t;
-            const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos / a.block_size);
-            if (blk >= 0 && (int64_t)blk < a.num_blocks) {
-              const int64_t rowi = (int64_t)blk * a.block_size + pos % a.block_size;
-              src[k] = (kv ? vc : kc) + rowi * row_elems + slab_off;
-              ++ok_rows;
-            } else if (kv == 0) {
-              set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
-            }
-          }
-        }
-      }
-      }
-      const int total_rows = __reduce_add_sync(0xffffffffu, ok_rows);
-      const bool first = flags & kFlagFirst;
-      const uint32_t bytes = (uint32_t)total_rows * C::ROW + (first ? C::Q_BYTES : 0);
-
-      if (it >= C::STAGES) {
-        if (!mbar_wait(&ctl.empty[s], (uint32_t)(((it / C::STAGES) - 1) & 1), abort_flag)) {
-          if (lane == 0) {
-            ctl.abort = 1;
-            set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
-          }
-        }
-      }
-      unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
-      if (lane == 0) {
-        StageMeta& m = ctl.meta[s];
-        m.pb = pb;
-        m.b = b;
-        m.tok0 = tok0;
-        m.count = count;
-        m.nb = nb;
-        m.flags = flags;
-        mbar_arrive_expect_tx(&ctl.full[s], bytes);
-      }
-      __syncwarp();
-      if (one_run) {
-        if (src[0] != nullptr)
-          bulk_g2s_hint(st + lane * C::KV_BYTES, src[0], (uint32_t)count * C::ROW, &ctl.full[s],
-                        policy);
-      } else {
-#pragma unroll
-      for (int k = 0; k < ROWS_PER_LANE; ++k) {
-        const int r = lane + 32 * k;
-        if (src[k] != nullptr) {
-          const int kv = r >= T;
-          const int t = kv ? r - T : r;
-          bulk_g2s_hint(st + kv * C::KV_BYTES + t * C::ROW, src[k], C::ROW, &ctl.full[s], policy);
-        }
-      }
-      }
-      if (first && lane == 0) {
-        const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) +
-                               ((int64_t)b * H + (int64_t)slab * HS * G) * kHeadDim;
-        bulk_g2s(st + 2 * C::KV_BYTES, qsrc, C::Q_BYTES, &ctl.full[s]);
-      }
-    }
-    // drain: the last issued stages must land before the CTA may exit
-    const int64_t first_drain = n_tiles > C::STAGES ? n_tiles - C::STAGES : 0;
-    for (int64_t it = first_drain; it < n_tiles; ++it) {
-      const int s = (int)(it % C::STAGES);
-      mbar_wait(&ctl.full[s], (uint32_t)((it / C::STAGES) & 1), abort_flag);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------------- consumers
-  const int j = warp / C::WPH;  // KV head within the slab
-  const int w = warp % C::WPH;  // token group within the tile
-  const int half = lane >> 4;
-  const int sub = lane & 15;
-  const int kvh = slab * HS + j;  // global KV head
-  const int kb = bfly_base<C::NV>(sub);
-  float* pbuf = pbuf_all + warp * C::PBUF_FLOATS;
-
-  float2 qp[G][4];  // q of the group's heads, this lane's 8 dims, pre-scaled
-  float2 op[G][4];  // running output, this lane's 8 dims
-  float m_run[G];
-  float m_own[C::CF];
-  float l_loc[C::CF];
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    m_run[hh] = -INFINITY;
-#pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = make_float2(0.f, 0.f), qp[hh][c2] = op[hh][c2];
-  }
-#pragma unroll
-  for (int r = 0; r < C::CF; ++r) m_own[r] = -INFINITY, l_loc[r] = 0.f;
-  const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
-
-  int seg_count = 0;
-  for (int64_t it = 0; it < n_tiles; ++it) {
-    const int s = (int)(it % C::STAGES);
-    if (!mbar_wait(&ctl.full[s], (uint32_t)((it / C::STAGES) & 1), abort_flag)) {
-      if (lane == 0) {
-        ctl.abort = 1;
-        set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
-      }
-    }
-    const StageMeta meta = ctl.meta[s];
-    const unsigned char* Kst = smem + (size_t)s * C::STAGE_BYTES;
-    const unsigned char* Vst = Kst + C::KV_BYTES;
-    const int count = meta.count;
-
-    if (meta.flags & kFlagFirst) {
-      const unsigned char* Qst = Kst + 2 * C::KV_BYTES;
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(Qst + ((j * G + hh) * kHeadDim + sub * 8) * 2);
-        qp[hh][0] = mul2(bf16x2_f2(qv.x), scale2);
-        qp[hh][1] = mul2(bf16x2_f2(qv.y), scale2);
-        qp[hh][2] = mul2(bf16x2_f2(qv.z), scale2);
-        qp[hh][3] = mul2(bf16x2_f2(qv.w), scale2);
-#pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = make_float2(0.f, 0.f);
-        m_run[hh] = -INFINITY;
-      }
-#pragma unroll
-      for (int r = 0; r < C::CF; ++r) m_own[r] = -INFINITY, l_loc[r] = 0.f;
-    }
-
-    // ---- this warp's rows of the tile: K now, V early (in-bounds shared loads) ---------
-    uint4 kraw[kPairs], vraw[kPairs];
-#pragma unroll
-    for (int i = 0; i < kPairs; ++i) {
-      const int t = w * kTokPerWarp + 2 * i + half;
-      const size_t off = (size_t)(t * HS + j) * (kHeadDim * 2) + sub * 16;
-      kraw[i] = *reinterpret_cast<const uint4*>(Kst + off);
-      vraw[i] = *reinterpret_cast<const uint4*>(Vst + off);
-      if (t >= count) vraw[i] = make_uint4(0u, 0u, 0u, 0u);  // stale rows must not reach p*v
-    }
-
-    // ---- scores: q . k, 8 dims per lane, reduced over the 16 lanes of a row ------------
-    float sc[C::NV];
-#pragma unroll
-    for (int i = 0; i < kPairs; ++i) {
-      const float2 k0 = bf16x2_f2(kraw[i].x), k1 = bf16x2_f2(kraw[i].y);
-      const float2 k2 = bf16x2_f2(kraw[i].z), k3 = bf16x2_f2(kraw[i].w);
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float2 acc = mul2(qp[hh][0], k0);
-        acc = fma2(qp[hh][1], k1, acc);
-        acc = fma2(qp[hh][2], k2, acc);
-        acc = fma2(qp[hh][3], k3, acc);
-        sc[i * G + hh] = acc.x + acc.y;
-      }
-    }
-    bfly<C::NV>(sc, sub, 8);
-    bfly<Half<C::NV>::v>(sc, sub, 4);
-    bfly<Half<Half<C::NV>::v>::v>(sc, sub, 2);
-    bfly<Half<Half<Half<C::NV>::v>::v>::v>(sc, sub, 1);
-
-    // ---- online softmax --------------------------------------------------------------
-    float tm[C::CF];
-    bool valid[C::CF];
-#pragma unroll
-    for (int r = 0; r < C::CF; ++r) {
-      const int kk = kb + r;
-      const int i = kk / G;
-      const int t = w * kTokPerWarp + 2 * i + half;
-      valid[r] = t < count;
-      sc[r] = valid[r] ? sc[r] : -INFINITY;
-      float v = sc[r];
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      tm[r] = v;
-    }
-    float alpha[G];
-    bool rescale = false;
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float t_max = head_bcast<G, C::CF>(tm, hh, lane);
-      const float m_new = fmaxf(m_run[hh], t_max);
-      alpha[hh] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run[hh] - m_new);
-      rescale |= (m_new != m_run[hh]);
-      m_run[hh] = m_new;
-    }
-#pragma unroll
-    for (int r = 0; r < C::CF; ++r) {
-      const float m_new = fmaxf(m_own[r], tm[r]);
-      const float al = (m_new == -INFINITY) ? 1.f : fast_exp2(m_own[r] - m_new);
-      const float p = valid[r] ? fast_exp2(sc[r] - m_new) : 0.f;
-      l_loc[r] = l_loc[r] * al + p;
-      m_own[r] = m_new;
-      pbuf[half * kPairs * G + kb + r] = p;
-    }
-    __syncwarp();
-    float pv[kPairs * G];
-#pragma unroll
-    for (int k = 0; k < kPairs * G / 4; ++k) {
-      const float4 f = *reinterpret_cast<const float4*>(pbuf + half * kPairs * G + 4 * k);
-      pv[4 * k + 0] = f.x;
-      pv[4 * k + 1] = f.y;
-      pv[4 * k + 2] = f.z;
-      pv[4 * k + 3] = f.w;
-    }
-    __syncwarp();
-    if (rescale) {
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float2 al2 = make_float2(alpha[hh], alpha[hh]);
-#pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = mul2(op[hh][c2], al2);
-      }
-    }
-    // ---- o += p v ----------------------------------------------------------------------
-#pragma unroll
-    for (int i = 0; i < kPairs; ++i) {
-      const float2 v0 = bf16x2_f2(vraw[i].x), v1 = bf16x2_f2(vraw[i].y);
-      const float2 v2 = bf16x2_f2(vraw[i].z), v3 = bf16x2_f2(vraw[i].w);
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float2 p2 = make_float2(pv[i * G + hh], pv[i * G + hh]);
-        op[hh][0] = fma2(p2, v0, op[hh][0]);
-        op[hh][1] = fma2(p2, v1, op[hh][1]);
-        op[hh][2] = fma2(p2, v2, op[hh][2]);
-        op[hh][3] = fma2(p2, v3, op[hh][3]);
-      }
-    }
-
-    if (meta.flags & kFlagLast) {
-      // ---- finalize the segment ----------------------------------------------------
-      // (1) fold the two half-warps (tokens 2i and 2i+1) and total the softmax sums
-      float o[G][8];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) {
-          o[hh][2 * c2] = op[hh][c2].x + __shfl_xor_sync(0xffffffffu, op[hh][c2].x, 16);
-          o[hh][2 * c2 + 1] = op[hh][c2].y + __shfl_xor_sync(0xffffffffu, op[hh][c2].y, 16);
-        }
-      float lt[C::CF];
-#pragma unroll
-      for (int r = 0; r < C::CF; ++r) {
-        float v = l_loc[r];
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        lt[r] = v;
-      }
-      float l_all[G];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) l_all[hh] = head_bcast<G, C::CF>(lt, hh, lane);
-
-      // (2) several warps per KV head (slabs below 8 heads): once every consumer warp is
-      // done with this stage's K/V, reuse it as scratch to merge their softmax states
-      if constexpr (C::WPH > 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.seg_bar);
-        if (!mbar_wait(&ctl.seg_bar, (uint32_t)(seg_count & 1), abort_flag)) {
-          if (lane == 0) {
-            ctl.abort = 1;
-            set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
-          }
-        }
-      }
-      float* merge = reinterpret_cast<float*>(smem + (size_t)s * C::STAGE_BYTES) +
-                     (size_t)j * (C::WPH - 1) * C::MERGE_FLOATS;
-      if (w != 0) {
-        float* mine = merge + (size_t)(w - 1) * C::MERGE_FLOATS;
-        if (half == 0) {
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float4* d4 = reinterpret_cast<float4*>(mine + hh * kHeadDim + sub * 8);
-            d4[0] = make_float4(o[hh][0], o[hh][1], o[hh][2], o[hh][3]);
-            d4[1] = make_float4(o[hh][4], o[hh][5], o[hh][6], o[hh][7]);
-          }
-        }
-        if (lane == 0) {
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            mine[G * kHeadDim + hh] = m_run[hh];
-            mine[G * kHeadDim + G + hh] = l_all[hh];
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.merge_bar[j]);
-      } else {
-        if constexpr (C::WPH > 1) {
-          if (!mbar_wait(&ctl.merge_bar[j], (uint32_t)(seg_count & 1), abort_flag)) {
-            if (lane == 0) {
-              ctl.abort = 1;
-              set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
-            }
-          }
-        }
-        for (int w2 = 1; w2 < C::WPH; ++w2) {
-          const float* other = merge + (size_t)(w2 - 1) * C::MERGE_FLOATS;
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const float m2 = other[G * kHeadDim + hh];
-            const float l2 = other[G * kHeadDim + G + hh];
-            const float mm = fmaxf(m_run[hh], m2);
-            const float a1 = (mm == -INFINITY) ? 0.f : fast_exp2(m_run[hh] - mm);
-            const float a2 = (mm == -INFINITY) ? 0.f : fast_exp2(m2 - mm);
-            const float4 p0 = lds128f(other + hh * kHeadDim + sub * 8);
-            const float4 p1 = lds128f(other + hh * kHeadDim + sub * 8 + 4);
-            const float ov[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[hh][e] = o[hh][e] * a1 + ov[e] * a2;
-            l_all[hh] = l_all[hh] * a1 + l2 * a2;
-            m_run[hh] = mm;
-          }
-        }
-        // (3) normalise and write the row, or the partial for the combine
-        const int b = meta.b;
-        if (meta.flags & kFlagWhole) {
-          if (half == 0) {
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const int hg = kvh * G + hh;
-              const float inv = l_all[hh] > 0.f ? 1.f / l_all[hh] : 0.f;
-              uint4 pk;
-              pk.x = f32x2_to_bf16x2(o[hh][0] * inv, o[hh][1] * inv);
-              pk.y = f32x2_to_bf16x2(o[hh][2] * inv, o[hh][3] * inv);
-              pk.z = f32x2_to_bf16x2(o[hh][4] * inv, o[hh][5] * inv);
-              pk.w = f32x2_to_bf16x2(o[hh][6] * inv, o[hh][7] * inv);
-              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                        ((int64_t)b * H + hg) * kHeadDim + sub * 8) = pk;
-            }
-          }
-        } else {
-          const int slot = (x0 < meta.pb) ? 1 : 0;
-          if (half == 0) {
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const int hg = kvh * G + hh;
-              const float inv = l_all[hh] > 0.f ? 1.f / l_all[hh] : 0.f;
-              float4* d4 = reinterpret_cast<float4*>(
-                  a.part_o + (((int64_t)c * 2 + slot) * H + hg) * kHeadDim + sub * 8);
-              d4[0] = make_float4(o[hh][0] * inv, o[hh][1] * inv, o[hh][2] * inv, o[hh][3] * inv);
-              d4[1] = make_float4(o[hh][4] * inv, o[hh][5] * inv, o[hh][6] * inv, o[hh][7] * inv);
-            }
-          }
-          if (lane == 0) {
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const int hg = kvh * G + hh;
-              a.part_lse[((int64_t)c * 2 + slot) * H + hg] =
-                  (l_all[hh] > 0.f) ? m_run[hh] + fast_log2(l_all[hh]) : -INFINITY;
-            }
-          }
-          __threadfence();
-          __syncwarp();
-          int old = 0;
-          int* counter = a.counters + (int64_t)b * Hk + kvh;
-          if (lane == 0) old = atomicAdd(counter, 1);
-          old = __shfl_sync(0xffffffffu, old, 0);
-          const int64_t c_lo = cta_of(meta.pb, NT, g_eff);
-          const int64_t c_hi = cta_of(meta.pb + meta.nb - 1, NT, g_eff);
-          const int nseg = (int)(c_hi - c_lo + 1);
-          if (old == nseg - 1) {
-            // (4) last arrival: combine the partials of sequence b in CTA order
-            __threadfence();
-#pragma unroll 1
-            for (int hh = 0; hh < G; ++hh) {
-              const int hg = kvh * G + hh;
-              float mx = -INFINITY;
-              for (int k0 = 0; k0 < nseg; k0 += 32) {
-                const int64_t c2 = c_lo + k0 + lane;
-                if (k0 + lane < nseg) {
-                  const int sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
-                  mx = fmaxf(mx, __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg));
-                }
-              }
-#pragma unroll
-              for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-              float den = 0.f;
-              for (int k0 = 0; k0 < nseg; k0 += 32) {
-                const int64_t c2 = c_lo + k0 + lane;
-                float wgt = 0.f;
-                int sl = 0;
-                if (k0 + lane < nseg) {
-                  sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
-                  const float ls = __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg);
-                  wgt = (mx == -INFINITY || ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
-                }
-                const int nk = min(32, nseg - k0);
-                for (int k = 0; k < nk; ++k) {
-                  const float wk = __shfl_sync(0xffffffffu, wgt, k);
-                  const int slk = __shfl_sync(0xffffffffu, sl, k);
-                  const int64_t ck = c_lo + k0 + k;
-                  den += wk;
-                  if (wk != 0.f) {
-                    const float4 po = __ldcg(reinterpret_cast<const float4*>(
-                        a.part_o + ((ck * 2 + slk) * H + hg) * kHeadDim) + lane);
-                    acc.x = fmaf(wk, po.x, acc.x);
-                    acc.y = fmaf(wk, po.y, acc.y);
-                    acc.z = fmaf(wk, po.z, acc.z);
-                    acc.w = fmaf(wk, po.w, acc.w);
-                  }
-                }
-              }
-              const float inv = den > 0.f ? 1.f / den : 0.f;
-              uint2 pk;
-              pk.x = f32x2_to_bf16x2(acc.x * inv, acc.y * inv);
-              pk.y = f32x2_to_bf16x2(acc.z * inv, acc.w * inv);
-              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) +
-                                        ((int64_t)b * H + hg) * kHeadDim + lane * 4) = pk;
-            }
-            if (lane == 0) *counter = 0;  // leave the counter zero for the next call
-          }
-        }
-      }
-      ++seg_count;
-      fence_proxy_async_smem();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl.empty[s]);
-  }
-}
-
-template <int HS, int G>
-int launch_decode_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
-  using C = DecCfg<HS, G>;
-  static bool attr_done[64] = {false};
-  const int dev = info.device;
-  if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<HS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_done[dev] = true;
-  }
-  const int slabs = a.num_kv_heads / HS;
-  dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);
-  paged_decode_kernel<HS, G><<<grid, kThreads, C::SMEM, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-}
-
-template <int HS>
-int dispatch_group(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
-  switch (a.num_heads / a.num_kv_heads) {
-    case 1: return launch_decode_t<HS, 1>(a, info, stream);
-    case 2: return launch_decode_t<HS, 2>(a, info, stream);
-    case 4: return launch_decode_t<HS, 4>(a, info, stream);
-    case 8: return launch_decode_t<HS, 8>(a, info, stream);
-    default: return PA_ERR_UNSUPPORTED;
-  }
-}
-
-}  // namespace
 
 int decode_head_slab(int num_kv_heads) {
   if (num_kv_heads % 8 == 0) return 8;
@@ -827,18 +26,21 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
   const size_t counters = up((size_t)num_seqs * num_kv_heads * sizeof(int));
   const size_t lse = up((size_t)max_ctas * 2 * num_heads * sizeof(float));
   const size_t o = up((size_t)max_ctas * 2 * num_heads * kHeadDim * sizeof(float));
-  *off_counters = 0;
-  *off_lse = counters;
-  *off_o = counters + lse;
-  *total = counters + lse + o;
+  // partials first, counters last: the counters' offset depends on the SM count and
+  // num_heads only, so a workspace sized for B sequences serves every call with fewer
+  // (same heads) and always finds its counters zero
+  *off_lse = 0;
+  *off_o = lse;
+  *off_counters = lse + o;
+  *total = lse + o + counters;
 }
 
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
   switch (decode_head_slab(a.num_kv_heads)) {
-    case 8: return dispatch_group<8>(a, info, stream);
-    case 4: return dispatch_group<4>(a, info, stream);
-    case 2: return dispatch_group<2>(a, info, stream);
-    default: return dispatch_group<1>(a, info, stream);
+    case 8: return dispatch_group<8, false>(a, info, stream);
+    case 4: return dispatch_group<4, false>(a, info, stream);
+    case 2: return dispatch_group<2, false>(a, info, stream);
+    default: return dispatch_group<1, false>(a, info, stream);
   }
 }
 

@@ -83,7 +83,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (cudaMemsetAsync(ws + off_c, 0, (size_t)num_seqs * num_kv_heads * sizeof(int), st) !=
       cudaSuccess)
     return PA_ERR_CUDA;
-  pa::DecodeArgs a;
+  pa::DecodeArgs a{};
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;

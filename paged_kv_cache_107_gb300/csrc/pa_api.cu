@@ -90,36 +90,61 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
   return total;
 }
 
-int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-              int64_t num_blocks, float scale, int grid_ctas, void* workspace,
-              size_t workspace_bytes, int* dev_err, void* stream) {
+}  // extern "C"
+
+namespace pa {
+
+// pa_decode and pa_decode_step share validation and argument packing; `step` is null for
+// the plain call.
+struct StepInput {
+  const void* k_new;
+  const void* v_new;
+  int64_t k_new_stride;
+  int64_t v_new_stride;
+  const int32_t* slot_mapping;
+};
+
+static int decode_entry(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                        float scale, int grid_ctas, void* workspace, size_t workspace_bytes,
+                        int* dev_err, void* stream, const StepInput* step) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || grid_ctas < 0)
     return PA_ERR_SHAPE;
   if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
-  if (head_dim != pa::kHeadDimApi || !pa::decode_supported(num_heads, num_kv_heads))
+  if (head_dim != kHeadDimApi || !decode_supported(num_heads, num_kv_heads))
     return PA_ERR_UNSUPPORTED;
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (step) {
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (step->k_new_stride < row || step->v_new_stride < row) return PA_ERR_SHAPE;
+  }
   if (num_seqs == 0) return PA_OK;
+  if (step) {
+    if (!step->k_new || !step->v_new || !step->slot_mapping) return PA_ERR_NULL;
+    // rows move with bulk copies: 16-byte aligned starts
+    if (!aligned16(step->k_new) || !aligned16(step->v_new) || (step->k_new_stride & 7) ||
+        (step->v_new_stride & 7))
+      return PA_ERR_ALIGN;
+  }
   if (!out || !q || !k_cache || !v_cache || !context_lens) return PA_ERR_NULL;
   if (max_blocks_per_seq > 0 && !block_tables) return PA_ERR_NULL;
-  if (!pa::aligned16(out) || !pa::aligned16(q) || !pa::aligned16(k_cache) ||
-      !pa::aligned16(v_cache))
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PA_ERR_ALIGN;
-  pa::DeviceInfo info;
-  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
-  const int max_ctas = pa::decode_max_ctas(info);
+  DeviceInfo info;
+  if (!current_device_info(&info)) return PA_ERR_CUDA;
+  const int max_ctas = decode_max_ctas(info);
   if (grid_ctas == 0) grid_ctas = info.num_sms;
   if (grid_ctas > max_ctas) return PA_ERR_SHAPE;
   size_t off_c, off_l, off_o, total;
-  pa::decode_workspace_layout(num_seqs, num_heads, num_kv_heads, max_ctas, &off_c, &off_l,
-                              &off_o, &total);
+  decode_workspace_layout(num_seqs, num_heads, num_kv_heads, max_ctas, &off_c, &off_l, &off_o,
+                          &total);
   if (!workspace || workspace_bytes < total) return PA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return PA_ERR_ALIGN;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  pa::DecodeArgs a;
+  DecodeArgs a{};
   a.out = out;
   a.q = q;
   a.k_cache = k_cache;
@@ -132,13 +157,50 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   a.num_kv_heads = num_kv_heads;
   a.block_size = block_size;
   a.num_blocks = num_blocks;
-  a.scale_log2 = pa::resolve_scale(scale, head_dim);
+  a.scale_log2 = resolve_scale(scale, head_dim);
   a.grid_ctas = grid_ctas;
   a.counters = reinterpret_cast<int*>(ws + off_c);
   a.part_lse = reinterpret_cast<float*>(ws + off_l);
   a.part_o = reinterpret_cast<float*>(ws + off_o);
   a.dev_err = dev_err;
-  return pa::launch_decode(a, info, static_cast<cudaStream_t>(stream));
+  if (step) {
+    a.k_new = step->k_new;
+    a.v_new = step->v_new;
+    a.k_new_stride = step->k_new_stride;
+    a.v_new_stride = step->v_new_stride;
+    a.slot_mapping = step->slot_mapping;
+    return launch_decode_step(a, info, static_cast<cudaStream_t>(stream));
+  }
+  return launch_decode(a, info, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace pa
+
+extern "C" {
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+              size_t workspace_bytes, int* dev_err, void* stream) {
+  return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, scale, grid_ctas, workspace, workspace_bytes, dev_err,
+                          stream, nullptr);
+}
+
+int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
+                   int64_t k_new_stride, int64_t v_new_stride, void* k_cache, void* v_cache,
+                   const int32_t* slot_mapping, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                   int num_heads, int num_kv_heads, int head_dim, int block_size,
+                   int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+                   size_t workspace_bytes, int* dev_err, void* stream) {
+  const pa::StepInput step{k_new, v_new, k_new_stride, v_new_stride, slot_mapping};
+  return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, scale, grid_ctas, workspace, workspace_bytes, dev_err,
+                          stream, &step);
 }
 
 int pa_prefill_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,

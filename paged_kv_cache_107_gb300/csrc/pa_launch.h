@@ -43,6 +43,12 @@ struct DecodeArgs {
   float scale_log2;  // softmax scale * log2(e)
   int grid_ctas;     // CTAs along the key stream (per head slab)
   int* counters;     // [num_seqs * num_kv_heads]
+  // fused store (pa_decode_step only; null / 0 otherwise): token b's rows, its slot
+  const void* k_new;
+  const void* v_new;
+  int64_t k_new_stride;  // elements between tokens
+  int64_t v_new_stride;
+  const int32_t* slot_mapping;
   float* part_o;     // [max_ctas * 2 * num_heads * head_dim]
   float* part_lse;   // [max_ctas * 2 * num_heads]
   int* dev_err;
@@ -58,6 +64,9 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
 int decode_head_slab(int num_kv_heads);
 bool decode_supported(int num_heads, int num_kv_heads);
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+// The same kernel with the store of token b (k_new/v_new row b) at slot_mapping[b] fused in;
+// the caches are written, so a.k_cache / a.v_cache must point to writable memory.
+int launch_decode_step(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
 
 struct PrefillArgs {
   void* out;

@@ -28,7 +28,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("pa_store_kvcache", "pa_decode", "pa_decode_workspace_size",
+    for must in ("pa_store_kvcache", "pa_decode", "pa_decode_step", "pa_decode_workspace_size",
                  "pa_prefill_varlen", "pa_status_str", "pa_version"):
         assert must in names, names
 
@@ -74,6 +74,17 @@ def test_validation_without_launch(lib):
     rc = lib.pa_store_kvcache(None, None, ctypes.c_int64(1024), ctypes.c_int64(1024), None, None,
                               None, 0, 8, 128, 16, ctypes.c_int64(4), None, None)
     assert rc == 0
+    # fused step: token stride below one row; head_dim 64; zero sequences is a no-op
+    lib.pa_decode_step.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+
+    def step(kstride, head_dim, B):
+        return lib.pa_decode_step(vp, vp, vp, vp, i64(kstride), i64(1024), vp, vp, vp, vp, 1, vp,
+                                  B, 16, 8, head_dim, 16, i64(4), ctypes.c_float(0), 0, vp,
+                                  ctypes.c_size_t(1 << 20), None, None)
+    assert step(1000, 128, 2) == 2
+    assert step(1024, 64, 2) == 3
+    assert step(1024, 128, 0) == 0
     # prefill: max_seqlen_k beyond what the table maps
     lib.pa_prefill_varlen.restype = ctypes.c_int
     rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 256,

@@ -190,3 +190,24 @@ def test_full_size_prefix_sharing(bs):
     case = workloads.workload(4, block_size=bs)
     assert case.shared_blocks > 0
     run_case(case, check_store=False)
+
+
+def test_workspace_reused_across_batch_sizes():
+    """One workspace sized for 512 sequences serves calls with 4, 300, 64 and 512
+    sequences in turn (same heads): partial results of a small call never land where a
+    larger call keeps its arrival counters."""
+    ws = pk.DecodeWorkspace(512, 16, 8, 128)
+    rng = np.random.default_rng(611)
+    for i, B in enumerate((4, 300, 64, 512)):
+        lens = rng.integers(1, 700, size=B)
+        case = workloads.decode_case(lens, 16, 8, 128, 64, seed=612 + i)
+        dc = DeviceCase(case)
+        dc.store()
+        out = dc.decode(grid_ctas=0, workspace=ws)
+        assert dc.dev_err() == 0
+        ok, ov = oracle_after_store(case)
+        got = to_f64(out)
+        assert np.all(np.isfinite(got)), f"batch {B}: a row was never written"
+        ref = oracle.decode(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+                            case.context_lens)
+        assert_close(got, ref, f"batch {B}")

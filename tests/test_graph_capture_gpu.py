@@ -1,7 +1,8 @@
 """The decode step as the engine runs it ("3.6 ModelRunner、CUDA Graph 与性能基准",
-section 5): store + decode captured once in a CUDA graph for a batch-size bucket, then
-replayed with new inputs copied into static buffers; rows past the real batch are
-padding (slot_mapping = -1, context_lens = 0). Every replay must match the oracle."""
+section 5): store + decode (two launches, or the fused pa_decode_step) captured once in a
+CUDA graph for a batch-size bucket, then replayed with new inputs copied into static
+buffers; rows past the real batch are padding (slot_mapping = -1, context_lens = 0).
+Every replay must match the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -14,7 +15,8 @@ from tests.gpu_helpers import assert_close, bits, from_bits, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def test_decode_step_graph_replay_with_padding_rows():
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_step_graph_replay_with_padding_rows(fused):
     dev = torch.device("cuda")
     bucket, H, Hk, D, bs = 16, 16, 8, 128, 16
     maxb = 40
@@ -35,8 +37,12 @@ def test_decode_step_graph_replay_with_padding_rows():
     err = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
-        pk.pa_store_kvcache(k_new, v_new, kc, vc, slots, dev_err=err)
-        pk.pa_decode(out, q, kc, vc, bt, ctx, workspace=ws, dev_err=err)
+        if fused:
+            pk.pa_decode_step(out, q, k_new, v_new, kc, vc, slots, bt, ctx, workspace=ws,
+                              dev_err=err)
+        else:
+            pk.pa_store_kvcache(k_new, v_new, kc, vc, slots, dev_err=err)
+            pk.pa_decode(out, q, kc, vc, bt, ctx, workspace=ws, dev_err=err)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
