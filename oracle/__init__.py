@@ -59,6 +59,8 @@ def _load(path=None):
         lib.oracle_prefill.restype = i32
         lib.oracle_slot_of.argtypes = [p, i32, i64, i32]
         lib.oracle_slot_of.restype = i64
+        lib.oracle_staged_apply.argtypes = [p, i64, i64, i32, i32, p, p, p, p]
+        lib.oracle_staged_apply.restype = i32
         lib.oracle_max_threads.argtypes = [i32]
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -193,6 +195,26 @@ def prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, causa
                             float(scale), rp, nrows, int(nthreads))
     _check(rc, "prefill")
     return (out, lse) if return_lse else out
+
+
+def staged_write_apply(base, writes):
+    """Return a copy of the 2-D array `base` after the staged writes, applied in staging
+    order: each write is (row, start, values) and puts the values at row `row`, columns
+    start .. start+len(values)-1 ("Model Runner V2 设计文档", "4. StagedWriteTensor")."""
+    out = np.ascontiguousarray(np.array(base, copy=True))
+    if out.ndim != 2:
+        raise ValueError("base must be 2-D")
+    rows = np.array([int(w[0]) for w in writes], dtype=np.int64)
+    starts = np.array([int(w[1]) for w in writes], dtype=np.int64)
+    vals = [np.asarray(w[2], dtype=out.dtype).reshape(-1) for w in writes]
+    lens = np.array([len(v) for v in vals], dtype=np.int64)
+    flat = (np.ascontiguousarray(np.concatenate(vals)) if vals
+            else np.zeros(1, dtype=out.dtype))
+    rc = _load().oracle_staged_apply(_ptr(out), out.shape[0], out.shape[1], out.itemsize,
+                                     len(writes), _ptr(rows), _ptr(starts), _ptr(lens),
+                                     _ptr(flat))
+    _check(rc, "staged write")
+    return out
 
 
 def slot_of(block_table_row, pos: int, block_size: int) -> int:

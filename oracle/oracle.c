@@ -24,6 +24,9 @@
  *   - prefill: "nano-vllm解读", "如何适配不同请求不同序列长度" and "3.6 ModelRunner…",
  *     section 2: new token i of sequence s sits at absolute position c_s + i with
  *     c_s = k_s - n_s cached tokens; causal means keys t <= c_s + i.
+ *   - staged writes: "Model Runner V2 设计文档", section "4. StagedWriteTensor": each
+ *     staged write copies its values into one row of the tensor from a start column; the
+ *     writes take effect one after another, in the order they were staged.
  *
  * bf16 values arrive as raw uint16 bits; each is widened exactly to double.
  * Parity status: every function here is pinned by the CPU tests (closed forms,
@@ -273,4 +276,25 @@ int64_t oracle_slot_of(const int32_t* table, int max_blocks, int64_t pos, int bl
   int64_t logical_block = pos / block_size;
   if (pos < 0 || logical_block >= max_blocks || table[logical_block] < 0) return -1;
   return (int64_t)table[logical_block] * block_size + pos % block_size;
+}
+
+/*
+ * Staged writes applied in staging order to a row-major [rows, cols] tensor of
+ * elem_bytes-byte elements. Write w puts w_len[w] values (taken in turn from `values`)
+ * at row w_row[w], columns w_start[w] .. w_start[w]+w_len[w]-1. A write that leaves the
+ * tensor is an invalid input (ORC_BAD_SHAPE), nothing after it is applied.
+ */
+int oracle_staged_apply(unsigned char* base, int64_t rows, int64_t cols, int elem_bytes,
+                        int nwrites, const int64_t* w_row, const int64_t* w_start,
+                        const int64_t* w_len, const unsigned char* values) {
+  int64_t taken = 0;
+  for (int w = 0; w < nwrites; ++w) {
+    if (w_row[w] < 0 || w_row[w] >= rows || w_start[w] < 0 || w_len[w] < 0 ||
+        w_start[w] + w_len[w] > cols)
+      return ORC_BAD_SHAPE;
+    memcpy(base + (w_row[w] * cols + w_start[w]) * elem_bytes, values + taken * elem_bytes,
+           (size_t)(w_len[w] * elem_bytes));
+    taken += w_len[w];
+  }
+  return ORC_OK;
 }

@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_staged_write_cpu as sw
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -36,6 +37,14 @@ MUTANTS = [
      [pins.test_decode_single_key_returns_its_value, pins.test_decode_zero_query_is_mean_of_values]),
     ("store_ignores_minus_one", "if (slot == -1) continue;", "if (slot == -1) slot = 0;",
      [pins.test_store_slot_minus_one_leaves_cache_byte_identical]),
+    ("staged_start_shift", "memcpy(base + (w_row[w] * cols + w_start[w]) * elem_bytes",
+     "memcpy(base + (w_row[w] * cols + w_start[w] + 1) * elem_bytes",
+     [sw.test_oracle_reproduces_the_pages_usage_example]),
+    ("staged_row_pitch", "memcpy(base + (w_row[w] * cols + w_start[w]) * elem_bytes",
+     "memcpy(base + (w_row[w] * rows + w_start[w]) * elem_bytes",
+     [sw.test_oracle_reproduces_the_pages_usage_example]),
+    ("staged_values_not_advanced", "taken += w_len[w];", "taken += 0;",
+     [sw.test_oracle_later_write_wins_on_overlap]),
 ]
 
 
@@ -48,6 +57,9 @@ def _call(fn):
         return fn(True)
     if "bs" in params:
         return fn(4)
+    if "dtype" in params:
+        import numpy as np
+        return fn(np.int32)
     return fn()
 
 
