@@ -373,6 +373,96 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None):
             "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
 
 
+def measure_staged(dev, steps: int, warmup: int):
+    """Block-table update through StagedWriteTensor ("Model Runner V2 设计文档", section 4):
+    a [1024, 1000] int32 table on the device; each step appends one block id to 256
+    sequences (a decode step of 256 sequences). Timed: the apply kernel alone (CUDA
+    events), the whole apply_write (host staging + merge + pack + one H2D copy + kernel),
+    and, for comparison, a full H2D copy of the table from pinned memory."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300.staged import StagedWriteTensor, merge_runs, pack_runs
+
+    rng = np.random.default_rng(107400)
+    R, C, W = 1024, 1000, 256
+    init = np.full((R, C), -1, np.int32)
+    t = StagedWriteTensor((R, C), dtype=torch.int32, init=torch.from_numpy(init))
+    stream = torch.cuda.current_stream(dev)
+    rows_all = [rng.choice(R, size=W, replace=False) for _ in range(steps + warmup)]
+    col = np.zeros(R, np.int64)
+
+    def staged_step(i):
+        for r in rows_all[i]:
+            t.stage_write(int(r), int(col[r] % C), [int(rng.integers(1 << 20))])
+            col[r] += 1
+        t.apply_write(stream)
+
+    for i in range(warmup):
+        staged_step(i)
+    torch.cuda.synchronize(dev)
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    s_ev.record(stream)
+    for i in range(warmup, warmup + steps):
+        staged_step(i)
+    e_ev.record(stream)
+    torch.cuda.synchronize(dev)
+    host_ms = (time.perf_counter() - t0) * 1e3 / steps
+    apply_ms = s_ev.elapsed_time(e_ev) / steps
+    h2d_bytes = t.last_h2d_bytes
+
+    # the kernel alone, on a packed buffer already on the device
+    runs = merge_runs([(int(r), int(j), np.array([7], np.int32))
+                       for j, r in enumerate(rows_all[0])])
+    buf, lay = pack_runs(runs, 4)
+    dbuf = torch.from_numpy(buf).to(dev)
+    base = dbuf.data_ptr()
+    lib = pk.load_library()
+
+    def kernel():
+        rc = lib.pa_staged_write_apply(
+            t.gpu.data_ptr(), R, C, C, 4, base + lay["rows"], base + lay["starts"],
+            base + lay["offsets"], base + lay["values"], lay["num_writes"], lay["num_values"],
+            t.dev_err.data_ptr(), stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(f"pa_staged_write_apply returned {rc}")
+
+    for _ in range(max(warmup, 3)):
+        kernel()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        kernel()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    kernel_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    # full copy of the table for comparison
+    host_tab = torch.from_numpy(init).pin_memory()
+    for _ in range(3):
+        t.gpu.copy_(host_tab, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in ev2:
+        a.record(stream)
+        t.gpu.copy_(host_tab, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    full_ms = statistics.median(a.elapsed_time(b) for a, b in ev2)
+    if int(t.dev_err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(t.dev_err.item())} in the staged writes")
+    return {"workload": "block_table_1024x1000_int32_256_appends", "writes_per_step": W,
+            "kernel_us": kernel_ms * 1e3, "apply_write_device_us": apply_ms * 1e3,
+            "apply_write_host_us": host_ms * 1e3, "h2d_bytes_per_step": h2d_bytes,
+            "full_table_copy_us": full_ms * 1e3, "full_table_bytes": R * C * 4,
+            "bound": "launch latency (1 KB of values per step)"}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -523,6 +613,7 @@ def run_ours(args):
     }
     if not args.no_prefill:
         line["prefill"] = measure_prefill(dev, steps=min(args.steps, 20), warmup=args.warmup)
+        line["staged_write"] = measure_staged(dev, steps=min(args.steps, 50), warmup=args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(case, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["gbs"], "unit": "GB/s", "cores": cb["cores"],

@@ -63,7 +63,8 @@ enum pa_dev_error {
   PA_DEV_ERR_SLOT = 2,     /* slot_mapping entry outside [-1, num_blocks*block_size) */
   PA_DEV_ERR_CONTEXT = 4,  /* context length above max_blocks_per_seq*block_size, or negative */
   PA_DEV_ERR_TIMEOUT = 8,  /* a bounded pipeline wait gave up (the kernel returned early) */
-  PA_DEV_ERR_SEQLENS = 16  /* cu_seqlens not non-decreasing, or a sequence shape out of range */
+  PA_DEV_ERR_SEQLENS = 16, /* cu_seqlens not non-decreasing, or a sequence shape out of range */
+  PA_DEV_ERR_STAGED = 32   /* a staged run outside the tensor, or run offsets that decrease */
 };
 
 /* Human-readable name of a pa_status value. Never NULL. */
@@ -96,6 +97,36 @@ int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t
                      void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                      int* dev_err, void* stream);
+
+/*
+ * pa_staged_write_apply — apply a packed batch of staged runs to a device tensor.
+ * Source: "Model Runner V2 设计文档", section "4. StagedWriteTensor" (the tensor stays on
+ * the GPU; the host stages the differences, packs them into one contiguous buffer, copies
+ * it to the GPU and launches one kernel that applies them; used for block tables and
+ * other state written by both host and GPU).
+ *
+ *   base            device, [num_rows, row_stride] elements of elem_bytes bytes (1, 2, 4
+ *                   or 8; int32 for block tables); columns 0..num_cols-1 of each row are
+ *                   the tensor.
+ *   rows, starts    device, int32 [num_writes]: run w writes row rows[w] from column
+ *                   starts[w] on.
+ *   offsets         device, int32 [num_writes+1], non-decreasing, offsets[0] = 0,
+ *                   offsets[num_writes] = num_values: run w's values are
+ *                   values[offsets[w] .. offsets[w+1]).
+ *   values          device, [num_values] elements of elem_bytes bytes.
+ *
+ * Result: base[rows[w]][starts[w] + i] = values[offsets[w] + i] for every run w and
+ * i < offsets[w+1] - offsets[w]; nothing else changes. Runs must not overlap (a host
+ * staging buffer merges overlapping writes, later ones winning, before packing); elements
+ * that several runs write receive one of their values. A run outside the tensor (row out
+ * of range, start < 0, start + length > num_cols) or decreasing offsets set
+ * PA_DEV_ERR_STAGED and that run is not written. rows, starts, offsets and values may
+ * all point into one packed buffer (each array aligned to its element size).
+ */
+int pa_staged_write_apply(void* base, int64_t num_rows, int64_t num_cols, int64_t row_stride,
+                          int elem_bytes, const int32_t* rows, const int32_t* starts,
+                          const int32_t* offsets, const void* values, int num_writes,
+                          int64_t num_values, int* dev_err, void* stream);
 
 /*
  * pa_decode_workspace_size — bytes of scratch that pa_decode needs for num_seqs

@@ -19,11 +19,12 @@ import torch
 from . import build as _build
 
 __all__ = ["pa_store_kvcache", "pa_decode", "pa_decode_step", "pa_decode_workspace_size",
-           "pa_prefill_varlen", "pa_decode_noalloc",
+           "pa_prefill_varlen", "pa_decode_noalloc", "pa_staged_write_apply",
            "pa_status_str", "pa_version", "DecodeWorkspace", "library_path", "load_library",
            "PA_DEV_ERR"]
 
-PA_DEV_ERR = {"block_id": 1, "slot": 2, "context": 4, "timeout": 8, "seqlens": 16}
+PA_DEV_ERR = {"block_id": 1, "slot": 2, "context": 4, "timeout": 8, "seqlens": 16,
+              "staged": 32}
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +67,9 @@ def load_library(path: Optional[str] = None):
         lib.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, i32, vp, i32,
                                        i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp]
         lib.pa_decode_step.restype = i32
+        lib.pa_staged_write_apply.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, i32, i64,
+                                              vp, vp]
+        lib.pa_staged_write_apply.restype = i32
         lib.pa_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                           i32, i32, i64, i32, f32, vp, vp]
         lib.pa_prefill_varlen.restype = i32
@@ -126,6 +130,28 @@ def pa_store_kvcache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
         _ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache), _ptr(v_cache),
         _ptr(slot_mapping), k.shape[0], hk, d, bs, nb, _ptr(dev_err), _stream(stream))
     _check(rc, "pa_store_kvcache")
+
+
+def pa_staged_write_apply(base: torch.Tensor, rows: torch.Tensor, starts: torch.Tensor,
+                          offsets: torch.Tensor, values: torch.Tensor,
+                          dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """base [R, C] device tensor (rows may be strided, columns contiguous); rows, starts
+    int32 [W]; offsets int32 [W+1]; values [offsets[W]] of base's element size. Run w
+    writes values[offsets[w]:offsets[w+1]] to base[rows[w], starts[w]:...]."""
+    if base.dim() != 2 or base.stride(1) != 1:
+        raise PagedAttentionError("base must be 2-D with contiguous columns")
+    for name, t in (("rows", rows), ("starts", starts), ("offsets", offsets)):
+        _need(t, name, torch.int32, 1)
+    if values.element_size() != base.element_size() or values.dim() != 1:
+        raise PagedAttentionError("values must be 1-D with base's element size")
+    W = rows.shape[0]
+    if starts.shape[0] != W or offsets.shape[0] != W + 1:
+        raise PagedAttentionError("rows / starts / offsets sizes disagree")
+    rc = load_library().pa_staged_write_apply(
+        _ptr(base), base.shape[0], base.shape[1], base.stride(0), base.element_size(),
+        _ptr(rows), _ptr(starts), _ptr(offsets), _ptr(values), W, values.shape[0],
+        _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_staged_write_apply")
 
 
 def pa_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,

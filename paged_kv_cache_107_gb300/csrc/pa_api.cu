@@ -79,6 +79,29 @@ int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t
                                   static_cast<cudaStream_t>(stream), info.num_sms);
 }
 
+int pa_staged_write_apply(void* base, int64_t num_rows, int64_t num_cols, int64_t row_stride,
+                          int elem_bytes, const int32_t* rows, const int32_t* starts,
+                          const int32_t* offsets, const void* values, int num_writes,
+                          int64_t num_values, int* dev_err, void* stream) {
+  if (num_rows < 0 || num_cols < 0 || row_stride < num_cols || num_writes < 0 || num_values < 0)
+    return PA_ERR_SHAPE;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return PA_ERR_UNSUPPORTED;
+  if (num_values > INT32_MAX) return PA_ERR_UNSUPPORTED;  // offsets are int32
+  if (num_values == 0) return PA_OK;
+  if (num_writes == 0) return PA_ERR_SHAPE;  // values without a run to hold them
+  if (!base || !rows || !starts || !offsets || !values) return PA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(base) | reinterpret_cast<uintptr_t>(values)) %
+          (uintptr_t)elem_bytes !=
+      0)
+    return PA_ERR_ALIGN;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
+  return pa::launch_staged_write(base, num_rows, num_cols, row_stride, elem_bytes, rows, starts,
+                                 offsets, values, num_writes, num_values, dev_err,
+                                 static_cast<cudaStream_t>(stream), info.num_sms);
+}
+
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim != pa::kHeadDimApi)
     return 0;

@@ -27,6 +27,11 @@ int launch_store_kvcache(const void* k, const void* v, int64_t k_tok_stride,
                          int head_dim, int64_t num_slots, int* dev_err, cudaStream_t stream,
                          int num_sms);
 
+int launch_staged_write(void* base, int64_t num_rows, int64_t num_cols, int64_t row_stride,
+                        int elem_bytes, const int32_t* rows, const int32_t* starts,
+                        const int32_t* offsets, const void* values, int num_writes,
+                        int64_t num_values, int* dev_err, cudaStream_t stream, int num_sms);
+
 struct DecodeArgs {
   void* out;
   const void* q;
