@@ -376,88 +376,85 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None):
 def measure_staged(dev, steps: int, warmup: int):
     """Block-table update through StagedWriteTensor ("Model Runner V2 设计文档", section 4):
     a [1024, 1000] int32 table on the device; each step appends one block id to 256
-    sequences (a decode step of 256 sequences). Timed: the apply kernel alone (CUDA
-    events), the whole apply_write (host staging + merge + pack + one H2D copy + kernel),
-    and, for comparison, a full H2D copy of the table from pinned memory."""
+    sequences (a decode step of 256 sequences). Timed with CUDA events: the apply kernel
+    alone, and the one H2D copy of the packed buffer plus the kernel; on the host clock,
+    a whole apply_write (staging + native merge/pack + issue). For comparison, a full H2D
+    copy of the table from pinned memory."""
     import numpy as np
     import torch
 
     import paged_kv_cache_107_gb300 as pk
-    from paged_kv_cache_107_gb300.staged import StagedWriteTensor, merge_runs, pack_runs
+    from paged_kv_cache_107_gb300.staged import StagedWriteTensor, pack
 
     rng = np.random.default_rng(107400)
     R, C, W = 1024, 1000, 256
     init = np.full((R, C), -1, np.int32)
     t = StagedWriteTensor((R, C), dtype=torch.int32, init=torch.from_numpy(init))
     stream = torch.cuda.current_stream(dev)
-    rows_all = [rng.choice(R, size=W, replace=False) for _ in range(steps + warmup)]
-    col = np.zeros(R, np.int64)
+    n = steps + warmup
+    rows_all = [rng.choice(R, size=W, replace=False).astype(np.int32) for _ in range(n)]
+    ids_all = [rng.integers(1 << 20, size=W).astype(np.int32) for _ in range(n)]
+    col = np.zeros(R, np.int32)
 
-    def staged_step(i):
-        for r in rows_all[i]:
-            t.stage_write(int(r), int(col[r] % C), [int(rng.integers(1 << 20))])
-            col[r] += 1
-        t.apply_write(stream)
+    def cols_for(rows):
+        c = col[rows] % C
+        col[rows] += 1
+        return c
 
+    # host: a whole apply_write per step, the engine's way (arrays of rows, columns, ids)
     for i in range(warmup):
-        staged_step(i)
+        t.stage_writes(rows_all[i], cols_for(rows_all[i]), ids_all[i])
+        t.apply_write(stream)
     torch.cuda.synchronize(dev)
-    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
-    s_ev.record(stream)
-    for i in range(warmup, warmup + steps):
-        staged_step(i)
-    e_ev.record(stream)
-    torch.cuda.synchronize(dev)
+    for i in range(warmup, n):
+        t.stage_writes(rows_all[i], cols_for(rows_all[i]), ids_all[i])
+        t.apply_write(stream)
     host_ms = (time.perf_counter() - t0) * 1e3 / steps
-    apply_ms = s_ev.elapsed_time(e_ev) / steps
+    torch.cuda.synchronize(dev)
     h2d_bytes = t.last_h2d_bytes
 
-    # the kernel alone, on a packed buffer already on the device
-    runs = merge_runs([(int(r), int(j), np.array([7], np.int32))
-                       for j, r in enumerate(rows_all[0])])
-    buf, lay = pack_runs(runs, 4)
-    dbuf = torch.from_numpy(buf).to(dev)
-    base = dbuf.data_ptr()
+    # device: pre-packed buffers, then (copy + kernel) per step and the kernel alone
+    packed = []
+    for i in range(n):
+        buf, lay = pack(rows_all[i], cols_for(rows_all[i]), np.ones(W, np.int32), ids_all[i], 4)
+        h = torch.from_numpy(buf.copy()).pin_memory()
+        packed.append((h, torch.empty(h.numel(), dtype=torch.uint8, device=dev), lay))
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in ev[warmup:])
+
+    def upload_apply(i):
+        h, d, lay = packed[i]
+        pk.pa_staged_upload_apply(t.gpu, h, d, lay, dev_err=t.dev_err, stream=stream)
+
     lib = pk.load_library()
 
-    def kernel():
+    def kernel(i):
+        _, d, lay = packed[i]
+        base = d.data_ptr()
         rc = lib.pa_staged_write_apply(
-            t.gpu.data_ptr(), R, C, C, 4, base + lay["rows"], base + lay["starts"],
-            base + lay["offsets"], base + lay["values"], lay["num_writes"], lay["num_values"],
-            t.dev_err.data_ptr(), stream.cuda_stream)
+            t.gpu.data_ptr(), R, C, C, 4, base + lay.rows_offset, base + lay.starts_offset,
+            base + lay.offsets_offset, base + lay.values_offset, lay.num_writes,
+            lay.num_values, t.dev_err.data_ptr(), stream.cuda_stream)
         if rc != 0:
             raise RuntimeError(f"pa_staged_write_apply returned {rc}")
 
-    for _ in range(max(warmup, 3)):
-        kernel()
-    torch.cuda.synchronize(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for a, b in ev:
-        a.record(stream)
-        kernel()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    kernel_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-
-    # full copy of the table for comparison
+    upload_ms = timed(upload_apply)
+    kernel_ms = timed(kernel)
     host_tab = torch.from_numpy(init).pin_memory()
-    for _ in range(3):
-        t.gpu.copy_(host_tab, non_blocking=True)
-    torch.cuda.synchronize(dev)
-    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for a, b in ev2:
-        a.record(stream)
-        t.gpu.copy_(host_tab, non_blocking=True)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    full_ms = statistics.median(a.elapsed_time(b) for a, b in ev2)
+    full_ms = timed(lambda i: t.gpu.copy_(host_tab, non_blocking=True))
     if int(t.dev_err.item()) != 0:
         raise RuntimeError(f"device error bits {int(t.dev_err.item())} in the staged writes")
     return {"workload": "block_table_1024x1000_int32_256_appends", "writes_per_step": W,
-            "kernel_us": kernel_ms * 1e3, "apply_write_device_us": apply_ms * 1e3,
+            "kernel_us": kernel_ms * 1e3, "upload_apply_device_us": upload_ms * 1e3,
             "apply_write_host_us": host_ms * 1e3, "h2d_bytes_per_step": h2d_bytes,
             "full_table_copy_us": full_ms * 1e3, "full_table_bytes": R * C * 4,
             "bound": "launch latency (1 KB of values per step)"}

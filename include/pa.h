@@ -116,8 +116,8 @@ int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t
  *   values          device, [num_values] elements of elem_bytes bytes.
  *
  * Result: base[rows[w]][starts[w] + i] = values[offsets[w] + i] for every run w and
- * i < offsets[w+1] - offsets[w]; nothing else changes. Runs must not overlap (a host
- * staging buffer merges overlapping writes, later ones winning, before packing); elements
+ * i < offsets[w+1] - offsets[w]; nothing else changes. Runs must not overlap
+ * (pa_staged_pack merges overlapping writes, later ones winning, before packing); elements
  * that several runs write receive one of their values. A run outside the tensor (row out
  * of range, start < 0, start + length > num_cols) or decreasing offsets set
  * PA_DEV_ERR_STAGED and that run is not written. rows, starts, offsets and values may
@@ -127,6 +127,47 @@ int pa_staged_write_apply(void* base, int64_t num_rows, int64_t num_cols, int64_
                           int elem_bytes, const int32_t* rows, const int32_t* starts,
                           const int32_t* offsets, const void* values, int num_writes,
                           int64_t num_values, int* dev_err, void* stream);
+
+/*
+ * Host-side staging for pa_staged_write_apply (no GPU involved): merges staged writes
+ * and packs them into one buffer that a single host-to-device copy moves.
+ *
+ * pa_staged_pack_bound — bytes that suffice to pack num_writes writes holding num_values
+ *   values in total (0 for invalid sizes).
+ * pa_staged_pack — write k (host arrays, staging order) puts lens[k] values (taken in
+ *   turn from `values`, elem_bytes each) at row rows[k] from column starts[k]. Writes of
+ *   one row that overlap or touch become one run; where they overlap the later write
+ *   wins. The runs go to `packed` (host memory, pinned for an asynchronous copy) as
+ *   int32 rows[W], starts[W], offsets[W+1], then the values at a 16-byte aligned offset;
+ *   *layout receives W, the value count, the byte offsets of the four arrays and the
+ *   total bytes. If packed_bytes is too small it returns PA_ERR_WORKSPACE with
+ *   layout->bytes set to the size needed. Negative lengths or starts: PA_ERR_SHAPE.
+ *   Rows and column bounds are checked on the device by pa_staged_write_apply.
+ */
+typedef struct pa_staged_layout {
+  int64_t rows_offset, starts_offset, offsets_offset, values_offset;
+  int32_t num_writes;
+  int64_t num_values;
+  int64_t bytes;
+} pa_staged_layout;
+
+size_t pa_staged_pack_bound(int num_writes, int64_t num_values, int elem_bytes);
+int pa_staged_pack(const int32_t* rows, const int32_t* starts, const int32_t* lens,
+                   const void* values, int num_writes, int elem_bytes, void* packed,
+                   size_t packed_bytes, pa_staged_layout* layout);
+
+/*
+ * pa_staged_upload_apply — one host-to-device copy of a packed buffer made by
+ * pa_staged_pack (layout->bytes bytes from packed_host to packed_dev, asynchronous on
+ * `stream`), then pa_staged_write_apply on the copy; base, num_rows, num_cols,
+ * row_stride, elem_bytes and dev_err as there. packed_dev is device memory of at least
+ * layout->bytes bytes, 16-byte aligned. packed_host should be pinned (page-locked) for
+ * the copy to be asynchronous; the caller keeps it unchanged until the copy has ended
+ * (an event recorded on `stream` after this call tells when).
+ */
+int pa_staged_upload_apply(void* base, int64_t num_rows, int64_t num_cols, int64_t row_stride,
+                           int elem_bytes, const void* packed_host, void* packed_dev,
+                           const pa_staged_layout* layout, int* dev_err, void* stream);
 
 /*
  * pa_decode_workspace_size — bytes of scratch that pa_decode needs for num_seqs

@@ -20,11 +20,15 @@ from . import build as _build
 
 __all__ = ["pa_store_kvcache", "pa_decode", "pa_decode_step", "pa_decode_workspace_size",
            "pa_prefill_varlen", "pa_decode_noalloc", "pa_staged_write_apply",
+           "pa_staged_pack", "pa_staged_pack_bound", "pa_staged_upload_apply",
+           "PaStagedLayout",
            "pa_status_str", "pa_version", "DecodeWorkspace", "library_path", "load_library",
            "PA_DEV_ERR"]
 
 PA_DEV_ERR = {"block_id": 1, "slot": 2, "context": 4, "timeout": 8, "seqlens": 16,
               "staged": 32}
+
+PA_ERR_WORKSPACE_CODE = 4
 
 _lock = threading.Lock()
 _lib = None
@@ -152,6 +156,74 @@ def pa_staged_write_apply(base: torch.Tensor, rows: torch.Tensor, starts: torch.
         _ptr(rows), _ptr(starts), _ptr(offsets), _ptr(values), W, values.shape[0],
         _ptr(dev_err), _stream(stream))
     _check(rc, "pa_staged_write_apply")
+
+
+class PaStagedLayout(ctypes.Structure):
+    """pa_staged_layout: byte offsets of the packed arrays, run and value counts."""
+    _fields_ = [("rows_offset", ctypes.c_int64), ("starts_offset", ctypes.c_int64),
+                ("offsets_offset", ctypes.c_int64), ("values_offset", ctypes.c_int64),
+                ("num_writes", ctypes.c_int32), ("num_values", ctypes.c_int64),
+                ("bytes", ctypes.c_int64)]
+
+
+def _staged_lib():
+    lib = load_library()
+    if not getattr(lib.pa_staged_pack, "_pa_typed", False):
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        lib.pa_staged_pack_bound.argtypes = [i32, i64, i32]
+        lib.pa_staged_pack_bound.restype = sz
+        lib.pa_staged_pack.argtypes = [vp, vp, vp, vp, i32, i32, vp, sz,
+                                       ctypes.POINTER(PaStagedLayout)]
+        lib.pa_staged_pack.restype = i32
+        lib.pa_staged_pack._pa_typed = True
+    return lib
+
+
+def pa_staged_pack_bound(num_writes: int, num_values: int, elem_bytes: int) -> int:
+    return int(_staged_lib().pa_staged_pack_bound(num_writes, num_values, elem_bytes))
+
+
+def pa_staged_pack(rows, starts, lens, values, elem_bytes: int, packed) -> PaStagedLayout:
+    """Native merge + pack (host code, no GPU): rows, starts, lens int32 numpy arrays and
+    values a numpy array of elem_bytes-byte elements, in staging order; `packed` a writable
+    host byte array (numpy, or the numpy view of a pinned tensor). Returns the layout;
+    raises with the needed size when `packed` is too small."""
+    import numpy as np
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    starts = np.ascontiguousarray(starts, dtype=np.int32)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    values = np.ascontiguousarray(values)
+    lay = PaStagedLayout()
+    rc = _staged_lib().pa_staged_pack(
+        rows.ctypes.data, starts.ctypes.data, lens.ctypes.data,
+        values.ctypes.data if values.size else None, len(rows), elem_bytes,
+        packed.ctypes.data, packed.nbytes, ctypes.byref(lay))
+    if rc == PA_ERR_WORKSPACE_CODE:
+        raise PagedAttentionError(f"pa_staged_pack: buffer too small, {lay.bytes} bytes needed")
+    _check(rc, "pa_staged_pack")
+    return lay
+
+
+def pa_staged_upload_apply(base: torch.Tensor, packed_host: torch.Tensor,
+                           packed_dev: torch.Tensor, layout: PaStagedLayout,
+                           dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One H2D copy of a packed buffer (pinned host uint8 tensor -> device uint8 tensor)
+    and the apply of its runs to `base` [R, C] (contiguous columns), on `stream`."""
+    lib = _staged_lib()
+    fn = lib.pa_staged_upload_apply
+    if not getattr(fn, "_pa_typed", False):
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        fn.argtypes = [vp, i64, i64, i64, i32, vp, vp, ctypes.POINTER(PaStagedLayout), vp, vp]
+        fn.restype = i32
+        fn._pa_typed = True
+    if base.dim() != 2 or base.stride(1) != 1:
+        raise PagedAttentionError("base must be 2-D with contiguous columns")
+    if packed_dev.numel() < layout.bytes or packed_host.numel() < layout.bytes:
+        raise PagedAttentionError("packed buffers smaller than layout.bytes")
+    rc = fn(base.data_ptr(), base.shape[0], base.shape[1], base.stride(0), base.element_size(),
+            packed_host.data_ptr(), packed_dev.data_ptr(), ctypes.byref(layout),
+            _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_staged_upload_apply")
 
 
 def pa_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,

@@ -102,6 +102,30 @@ int pa_staged_write_apply(void* base, int64_t num_rows, int64_t num_cols, int64_
                                  static_cast<cudaStream_t>(stream), info.num_sms);
 }
 
+int pa_staged_upload_apply(void* base, int64_t num_rows, int64_t num_cols, int64_t row_stride,
+                           int elem_bytes, const void* packed_host, void* packed_dev,
+                           const pa_staged_layout* layout, int* dev_err, void* stream) {
+  if (!layout) return PA_ERR_NULL;
+  if (num_rows < 0 || num_cols < 0 || row_stride < num_cols || layout->bytes < 0 ||
+      layout->num_writes < 0 || layout->num_values < 0)
+    return PA_ERR_SHAPE;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return PA_ERR_UNSUPPORTED;
+  if (layout->bytes == 0) return PA_OK;
+  if (!packed_host || !packed_dev || (layout->num_values > 0 && !base)) return PA_ERR_NULL;
+  if (layout->num_values > 0 && layout->num_writes == 0) return PA_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(packed_dev) & 15) ||
+      (reinterpret_cast<uintptr_t>(base) % (uintptr_t)elem_bytes) ||
+      (layout->values_offset % 16) || (layout->rows_offset % 4) || (layout->starts_offset % 4) ||
+      (layout->offsets_offset % 4))
+    return PA_ERR_ALIGN;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
+  return pa::launch_staged_upload_apply(base, num_rows, num_cols, row_stride, elem_bytes,
+                                        packed_host, packed_dev, layout, dev_err,
+                                        static_cast<cudaStream_t>(stream), info.num_sms);
+}
+
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim != pa::kHeadDimApi)
     return 0;

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/pa.h"
+
 namespace pa {
 
 // The only head_dim the kernels are built for.
@@ -31,6 +33,11 @@ int launch_staged_write(void* base, int64_t num_rows, int64_t num_cols, int64_t 
                         int elem_bytes, const int32_t* rows, const int32_t* starts,
                         const int32_t* offsets, const void* values, int num_writes,
                         int64_t num_values, int* dev_err, cudaStream_t stream, int num_sms);
+
+int launch_staged_upload_apply(void* base, int64_t num_rows, int64_t num_cols,
+                               int64_t row_stride, int elem_bytes, const void* packed_host,
+                               void* packed_dev, const pa_staged_layout* lay, int* dev_err,
+                               cudaStream_t stream, int num_sms);
 
 struct DecodeArgs {
   void* out;

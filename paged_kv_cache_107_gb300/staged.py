@@ -3,84 +3,71 @@
 "Model Runner V2 设计文档", section "4. StagedWriteTensor": the tensor (block tables,
 for instance) stays on the GPU; the host stages only the changed runs, packs them into
 one contiguous buffer, copies that buffer in one host-to-device copy and launches one
-kernel (pa_staged_write_apply) that applies them. No full copy of the tensor and no
-host-device synchronisation on the way.
+kernel that applies them. No full copy of the tensor and no host-device synchronisation.
 
-Host side only: staging, merging overlapping runs of the same row (later writes win, so
-the packed runs never overlap) and packing. Every element of the tensor is written by
-the CUDA kernel."""
+Merging and packing run in the library's native host code (pa_staged_pack), straight
+into a pinned buffer; the apply is the CUDA kernel behind pa_staged_write_apply. This
+module only collects the staged writes and passes pointers."""
 from __future__ import annotations
 
-from typing import Dict, List, Optional, Sequence, Tuple
+from typing import List, Optional, Tuple
 
 import numpy as np
 import torch
 
-from . import PagedAttentionError, _ptr, _stream, load_library
+from . import (PaStagedLayout, PagedAttentionError, pa_staged_pack, pa_staged_pack_bound,
+               pa_staged_upload_apply)
 
 _NP = {torch.int32: np.int32, torch.float32: np.float32, torch.int64: np.int64,
        torch.int16: np.int16, torch.uint8: np.uint8, torch.float64: np.float64}
 
 
-def merge_runs(staged: Sequence[Tuple[int, int, np.ndarray]]) -> List[Tuple[int, int, np.ndarray]]:
-    """Staged (row, start, values) writes, in staging order -> non-overlapping runs with
-    the same effect: within a row, a later write overrides an earlier one where they
-    overlap; runs that overlap or touch are joined. Output sorted by (row, start)."""
-    by_row: Dict[int, List[Tuple[int, np.ndarray]]] = {}
-    for row, start, vals in staged:
-        if len(vals):
-            by_row.setdefault(row, []).append((start, vals))
-    out = []
-    for row in sorted(by_row):
-        writes = by_row[row]
-        if len(writes) == 1:
-            out.append((row, writes[0][0], writes[0][1]))
-            continue
-        lo = min(s for s, _ in writes)
-        hi = max(s + len(v) for s, v in writes)
-        buf = np.zeros(hi - lo, dtype=writes[0][1].dtype)
-        mask = np.zeros(hi - lo, dtype=bool)
-        for s, v in writes:  # staging order: later writes land last
-            buf[s - lo:s - lo + len(v)] = v
-            mask[s - lo:s - lo + len(v)] = True
-        # maximal runs of covered columns
-        edges = np.flatnonzero(np.diff(np.concatenate(([0], mask.view(np.int8), [0]))))
-        for a, b in zip(edges[0::2], edges[1::2]):
-            out.append((row, lo + int(a), buf[a:b].copy()))
-    return out
+Layout = PaStagedLayout
 
 
-def pack_runs(runs: Sequence[Tuple[int, int, np.ndarray]], elem_bytes: int) -> Tuple[np.ndarray, dict]:
-    """One contiguous byte buffer: int32 rows[W], starts[W], offsets[W+1], then the values
-    (aligned to max(elem_bytes, 4)). Returns the buffer and the byte offsets of each part."""
-    W = len(runs)
-    lens = np.array([len(v) for _, _, v in runs], dtype=np.int64)
-    offsets = np.zeros(W + 1, dtype=np.int64)
-    np.cumsum(lens, out=offsets[1:])
-    if offsets[-1] > np.iinfo(np.int32).max:
-        raise PagedAttentionError("too many staged values for int32 offsets")
-    head = 4 * (3 * W + 1)
-    align = max(elem_bytes, 16)
-    val_off = (head + align - 1) // align * align
-    total = val_off + int(offsets[-1]) * elem_bytes
-    buf = np.zeros(total, dtype=np.uint8)
-    meta = buf[:head].view(np.int32)
-    meta[:W] = [r for r, _, _ in runs]
-    meta[W:2 * W] = [s for _, s, _ in runs]
-    meta[2 * W:3 * W + 1] = offsets
-    if W:
-        buf[val_off:] = np.concatenate([v for _, _, v in runs]).view(np.uint8)
-    return buf, {"rows": 0, "starts": 4 * W, "offsets": 8 * W, "values": val_off,
-                 "num_writes": W, "num_values": int(offsets[-1])}
+def pack(rows, starts, lens, values, elem_bytes: int, out: Optional[np.ndarray] = None):
+    """Native merge + pack of staged writes (numpy arrays, staging order). Returns the
+    packed bytes (a view of `out` when given) and the layout."""
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    need = pa_staged_pack_bound(len(lens), int(lens.sum()) if len(lens) else 0, elem_bytes)
+    if out is None or out.nbytes < need:
+        out = np.empty(max(need, 16), dtype=np.uint8)
+    lay = pa_staged_pack(rows, starts, lens, values, elem_bytes, out)
+    return out[:lay.bytes], lay
+
+
+def unpack(buf: np.ndarray, lay: Layout, dtype) -> List[Tuple[int, int, np.ndarray]]:
+    """The runs of a packed buffer as (row, start, values) (for tests and inspection)."""
+    W = lay.num_writes
+    rows = buf[lay.rows_offset:lay.rows_offset + 4 * W].view(np.int32)
+    starts = buf[lay.starts_offset:lay.starts_offset + 4 * W].view(np.int32)
+    offs = buf[lay.offsets_offset:lay.offsets_offset + 4 * (W + 1)].view(np.int32)
+    vals = buf[lay.values_offset:].view(dtype)
+    return [(int(rows[k]), int(starts[k]), vals[offs[k]:offs[k + 1]]) for k in range(W)]
+
+
+class _Slot:
+    """One pinned host buffer, its device copy target, and the event of its last copy."""
+
+    def __init__(self, nbytes: int, device):
+        self.host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        self.host_np = self.host.numpy()
+        self.dev = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.copied: Optional[torch.cuda.Event] = None
 
 
 class StagedWriteTensor:
     """A [rows, cols] tensor on the GPU with host-staged run writes.
 
-    stage_write(row, start, values) records a run on the host; apply_write() merges the
-    staged runs, packs them into one pinned buffer, copies it to the device in one copy and
-    applies it with one kernel launch on `stream`. Both calls return without waiting for
-    the GPU; the pinned buffer of a previous apply is reused only after its copy ended."""
+    stage_write(row, start, values) records one run; stage_writes(rows, starts, values,
+    lens) records many from arrays. apply_write() merges and packs them natively into a
+    pinned buffer, copies it to the device in one copy and applies it with one kernel
+    launch on `stream` (one native call for both). Neither call waits for the GPU: the
+    packed buffers form a ring of RING slots, and a slot is reused only once the copy it
+    last fed has ended (a wait that happens only when the ring wraps faster than the
+    GPU consumes it)."""
+
+    RING = 3
 
     def __init__(self, size: Tuple[int, int], dtype: torch.dtype = torch.int32,
                  device="cuda", init: Optional[torch.Tensor] = None):
@@ -92,42 +79,56 @@ class StagedWriteTensor:
             raise PagedAttentionError("StagedWriteTensor is 2-D")
         self.dtype = dtype
         self._np = _NP[dtype]
-        self._staged: List[Tuple[int, int, np.ndarray]] = []
-        self._pinned: Optional[torch.Tensor] = None
-        self._dev: Optional[torch.Tensor] = None
-        self._copied: Optional[torch.cuda.Event] = None
+        self._clear()
+        self._slots: List[Optional[_Slot]] = [None] * self.RING
+        self._next = 0
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=self.gpu.device)
         self.last_h2d_bytes = 0
 
+    def _clear(self):
+        self._rows, self._starts, self._lens, self._vals = [], [], [], []
+
     def stage_write(self, row: int, start: int, value) -> None:
-        self._staged.append((int(row), int(start), np.array(value, dtype=self._np).reshape(-1)))
+        v = np.array(value, dtype=self._np).reshape(-1)
+        self._rows.append(np.array([row], np.int32))
+        self._starts.append(np.array([start], np.int32))
+        self._lens.append(np.array([v.size], np.int32))
+        self._vals.append(v)
+
+    def stage_writes(self, rows, starts, values, lens=None) -> None:
+        """Many runs at once, in order: run k writes lens[k] values (default 1 each) taken
+        in turn from `values`."""
+        rows = np.asarray(rows, np.int32).reshape(-1)
+        lens = (np.ones(rows.size, np.int32) if lens is None
+                else np.asarray(lens, np.int32).reshape(-1))
+        self._rows.append(rows)
+        self._starts.append(np.asarray(starts, np.int32).reshape(-1))
+        self._lens.append(lens)
+        self._vals.append(np.asarray(values, dtype=self._np).reshape(-1))
 
     def apply_write(self, stream=None) -> None:
-        if not self._staged:
+        if not self._rows:
             return
-        runs = merge_runs(self._staged)
-        self._staged = []
-        buf, lay = pack_runs(runs, self.gpu.element_size())
-        n = buf.nbytes
-        if self._pinned is None or self._pinned.numel() < n:
-            cap = max(n, 4096)
-            self._pinned = torch.empty(cap, dtype=torch.uint8).pin_memory()
-            self._dev = torch.empty(cap, dtype=torch.uint8, device=self.gpu.device)
-            self._copied = None
-        if self._copied is not None:
-            self._copied.synchronize()  # the previous copy must have read the pinned buffer
-        self._pinned[:n].numpy()[:] = buf
+        one = len(self._rows) == 1
+        rows = self._rows[0] if one else np.concatenate(self._rows)
+        starts = self._starts[0] if one else np.concatenate(self._starts)
+        lens = self._lens[0] if one else np.concatenate(self._lens)
+        vals = self._vals[0] if one else np.concatenate(self._vals)
+        self._clear()
+        eb = self.gpu.element_size()
+        need = pa_staged_pack_bound(len(rows), int(lens.sum()), eb)
+        k = self._next
+        self._next = (k + 1) % self.RING
+        slot = self._slots[k]
+        if slot is None or slot.host.numel() < need:
+            slot = self._slots[k] = _Slot(max(need, 4096), self.gpu.device)
+        elif slot.copied is not None:
+            slot.copied.synchronize()  # its last copy must have read the pinned buffer
+        lay = pa_staged_pack(rows, starts, lens, vals, eb, slot.host_np)
         s = stream if stream is not None else torch.cuda.current_stream(self.gpu.device)
-        with torch.cuda.stream(s):
-            self._dev[:n].copy_(self._pinned[:n], non_blocking=True)
-            self._copied = torch.cuda.Event()
-            self._copied.record(s)
-        self.last_h2d_bytes = n
-        base = self._dev.data_ptr()
-        rc = load_library().pa_staged_write_apply(
-            _ptr(self.gpu), self.gpu.shape[0], self.gpu.shape[1], self.gpu.stride(0),
-            self.gpu.element_size(), base + lay["rows"], base + lay["starts"],
-            base + lay["offsets"], base + lay["values"], lay["num_writes"], lay["num_values"],
-            _ptr(self.dev_err), _stream(s))
-        if rc != 0:
-            raise PagedAttentionError(f"pa_staged_write_apply: {load_library().pa_status_str(rc).decode()}")
+        pa_staged_upload_apply(self.gpu, slot.host, slot.dev, lay, dev_err=self.dev_err,
+                               stream=s)
+        if slot.copied is None:
+            slot.copied = torch.cuda.Event()
+        slot.copied.record(s)
+        self.last_h2d_bytes = lay.bytes

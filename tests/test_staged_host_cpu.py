@@ -1,5 +1,6 @@
-"""CPU tests of the host staging (merge + pack) that feeds pa_staged_write_apply
-("Model Runner V2 设计文档", section "4. StagedWriteTensor"), checked against the oracle."""
+"""CPU tests of the library's native host staging (pa_staged_pack: merge + pack) that
+feeds pa_staged_write_apply ("Model Runner V2 设计文档", section "4. StagedWriteTensor"),
+checked against the oracle. No GPU: the packing is host code."""
 import numpy as np
 
 import oracle
@@ -19,7 +20,12 @@ def test_merged_runs_do_not_overlap_and_have_the_same_effect():
             s = int(rng.integers(C))
             n = int(rng.integers(0, C - s + 1))
             writes.append((r, s, rng.integers(-99, 99, size=n).astype(np.int32)))
-        runs = staged.merge_runs(writes)
+        rows = [w[0] for w in writes]
+        starts = [w[1] for w in writes]
+        lens = [len(w[2]) for w in writes]
+        vals = np.concatenate([w[2] for w in writes]) if writes else np.zeros(0, np.int32)
+        buf, lay = staged.pack(rows, starts, lens, vals, 4)
+        runs = staged.unpack(buf, lay, np.int32)
         cover = {}
         for r, s, v in runs:
             assert len(v) > 0
@@ -32,11 +38,29 @@ def test_merged_runs_do_not_overlap_and_have_the_same_effect():
 
 
 def test_pack_layout():
-    runs = [(2, 3, np.array([3, 1, 2], np.int32)), (0, 1, np.array([-1, -2, -5], np.int32))]
-    buf, lay = staged.pack_runs(runs, 4)
-    meta = buf[:4 * 7].view(np.int32)
-    assert meta[:2].tolist() == [2, 0]
-    assert meta[2:4].tolist() == [3, 1]
-    assert meta[4:7].tolist() == [0, 3, 6]
-    assert lay["values"] % 16 == 0 and lay["num_values"] == 6 and lay["num_writes"] == 2
-    assert buf[lay["values"]:].view(np.int32).tolist() == [3, 1, 2, -1, -2, -5]
+    """Two disjoint writes stay two runs, sorted by row; offsets and values as packed."""
+    buf, lay = staged.pack([2, 0], [3, 1], [3, 3], np.array([3, 1, 2, -1, -2, -5], np.int32), 4)
+    W = lay.num_writes
+    assert W == 2 and lay.num_values == 6 and lay.values_offset % 16 == 0
+    assert buf[:8].view(np.int32).tolist() == [0, 2]
+    assert buf[8:16].view(np.int32).tolist() == [1, 3]
+    assert buf[16:28].view(np.int32).tolist() == [0, 3, 6]
+    assert buf[lay.values_offset:].view(np.int32).tolist() == [-1, -2, -5, 3, 1, 2]
+
+
+def test_pack_joins_touching_and_overlapping_writes():
+    buf, lay = staged.pack([1, 1, 1], [0, 4, 2], [4, 2, 3],
+                           np.array([1, 2, 3, 4, 5, 6, 7, 8, 9], np.int64), 8)
+    runs = staged.unpack(buf, lay, np.int64)
+    assert len(runs) == 1
+    r, s0, v = runs[0]
+    assert (r, s0) == (1, 0) and v.tolist() == [1, 2, 7, 8, 9, 6]
+
+
+def test_pack_rejects_negative_lengths_and_reports_size():
+    import pytest
+    import paged_kv_cache_107_gb300 as pk
+    with pytest.raises(pk.PagedAttentionError):
+        staged.pack([0], [0], [-1], np.zeros(0, np.int32), 4)
+    with pytest.raises(pk.PagedAttentionError, match="28 bytes needed"):
+        pk.pa_staged_pack([0], [0], [3], np.array([1, 2, 3], np.int32), 4, np.zeros(8, np.uint8))

@@ -137,3 +137,22 @@ def test_long_runs():
     torch.cuda.synchronize()
     assert np.array_equal(t.gpu.cpu().numpy(),
                           oracle.staged_write_apply(np.zeros((R, C), np.int32), writes))
+
+
+@pytest.mark.parametrize("W", [8191, 8192, 20000])
+def test_run_counts_around_the_shared_memory_limit(W):
+    """Up to 8191 runs the offsets (W+1 entries) sit in shared memory; from 8192 runs
+    the search reads them from global memory: both paths give the oracle's result."""
+    rng = np.random.default_rng(W)
+    R, C = 4096, 64
+    t = StagedWriteTensor((R, C), dtype=torch.int32)
+    flat = rng.choice(R * C, size=W, replace=False)
+    rows, cols = (flat // C).astype(np.int32), (flat % C).astype(np.int32)
+    vals = rng.integers(-(1 << 31), 1 << 31, size=W).astype(np.int32)
+    t.stage_writes(rows, cols, vals)
+    t.apply_write()
+    torch.cuda.synchronize()
+    assert int(t.dev_err.item()) == 0
+    ref = oracle.staged_write_apply(np.zeros((R, C), np.int32),
+                                    [(int(r), int(c), [int(v)]) for r, c, v in zip(rows, cols, vals)])
+    assert np.array_equal(t.gpu.cpu().numpy(), ref)
