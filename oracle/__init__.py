@@ -61,6 +61,17 @@ def _load(path=None):
         lib.oracle_slot_of.restype = i64
         lib.oracle_staged_apply.argtypes = [p, i64, i64, i32, i32, p, p, p, p]
         lib.oracle_staged_apply.restype = i32
+        u32, u64 = ctypes.c_uint32, ctypes.c_uint64
+        lib.oracle_philox4x32_10.argtypes = [p, p, p]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_philox_bits.argtypes = [u64, u64, u64]
+        lib.oracle_philox_bits.restype = u32
+        lib.oracle_uniform.argtypes = [u32]
+        lib.oracle_uniform.restype = dbl
+        lib.oracle_gumbel_sample.argtypes = [p, p, p, p, i64, i32, i32, i64, p, p, p, i32]
+        lib.oracle_gumbel_sample.restype = i32
+        lib.oracle_gumbel_scores.argtypes = [p, p, i32, i64, ctypes.c_float, u64, u64]
+        lib.oracle_gumbel_scores.restype = i32
         lib.oracle_max_threads.argtypes = [i32]
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -214,6 +225,63 @@ def staged_write_apply(base, writes):
                                      len(writes), _ptr(rows), _ptr(starts), _ptr(lens),
                                      _ptr(flat))
     _check(rc, "staged write")
+    return out
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 (Salmon et al., SC 2011): four 32-bit counter words and two key words
+    -> four 32-bit outputs."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def philox_bits(seed: int, offset: int, i: int) -> int:
+    """The 32 random bits of vocabulary element i for a row's (seed, offset)."""
+    return int(_load().oracle_philox_bits(seed, offset, i))
+
+
+def uniform(bits: int) -> float:
+    """u = (2*(bits >> 9) + 1) / 2^24."""
+    return float(_load().oracle_uniform(bits))
+
+
+def _logits_arg(logits):
+    import torch
+    if isinstance(logits, torch.Tensor):
+        if logits.dtype == torch.bfloat16:
+            return _u16(logits), 1
+        logits = logits.numpy()
+    a = np.ascontiguousarray(logits, dtype=np.float32)
+    return a, 0
+
+
+def gumbel_sample(logits, temperatures, seeds, offsets, nthreads=0):
+    """Gumbel-max sample of each row of logits [B, V] (binary32, or a bf16 torch tensor):
+    returns (index int64 [B], best score [B], runner-up score [B]) in fp64."""
+    a, is_bf16 = _logits_arg(logits)
+    B, V = a.shape
+    t = np.ascontiguousarray(temperatures, dtype=np.float32)
+    sd = np.ascontiguousarray(seeds, dtype=np.uint64)
+    of = np.ascontiguousarray(offsets, dtype=np.uint64)
+    out = np.zeros(B, np.int64)
+    best = np.zeros(B, np.float64)
+    second = np.zeros(B, np.float64)
+    rc = _load().oracle_gumbel_sample(_ptr(out), _ptr(best), _ptr(second), _ptr(a), V, is_bf16,
+                                      B, V, _ptr(t), _ptr(sd), _ptr(of), int(nthreads))
+    _check(rc, "gumbel sample")
+    return out, best, second
+
+
+def gumbel_scores(row_logits, temperature: float, seed: int, offset: int):
+    """All fp64 scores logits/T - ln(-ln u) of one row (the logit alone when T <= 0)."""
+    a, is_bf16 = _logits_arg(row_logits)
+    a = a.reshape(-1)
+    out = np.zeros(a.shape[0], np.float64)
+    _load().oracle_gumbel_scores(_ptr(out), _ptr(a), is_bf16, a.shape[0], float(temperature),
+                                 int(seed), int(offset))
     return out
 
 

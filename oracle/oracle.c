@@ -24,6 +24,15 @@
  *   - prefill: "nano-vllm解读", "如何适配不同请求不同序列长度" and "3.6 ModelRunner…",
  *     section 2: new token i of sequence s sits at absolute position c_s + i with
  *     c_s = k_s - n_s cached tokens; causal means keys t <= c_s + i.
+ *   - Gumbel-max sampling: "nano-vllm解读", "Gumbel-Max采样": the sample of row b is
+ *     argmax_i (ln p_i + G_i), p = softmax(logits / T), G_i = -ln(-ln u_i) with u_i
+ *     independent U(0,1); ln p_i differs from logits_i / T by a constant of the row, so
+ *     the score used is logits_i / T + G_i. "Model Runner V2 设计文档", section 6
+ *     ("Gumbel 采样内核"): the uniforms come from a stateless generator keyed by a seed
+ *     input. The generator is Philox4x32-10 as published by Salmon, Moraes, Dror and
+ *     Shaw ("Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011); the use of its
+ *     counter, the uniform mapping and the greedy / NaN / tie rules are this library's
+ *     definitions, restated in gumbel_score below.
  *   - staged writes: "Model Runner V2 设计文档", section "4. StagedWriteTensor": each
  *     staged write copies its values into one row of the tensor from a start column; the
  *     writes take effect one after another, in the order they were staged.
@@ -295,6 +304,108 @@ int oracle_staged_apply(unsigned char* base, int64_t rows, int64_t cols, int ele
     memcpy(base + (w_row[w] * cols + w_start[w]) * elem_bytes, values + taken * elem_bytes,
            (size_t)(w_len[w] * elem_bytes));
     taken += w_len[w];
+  }
+  return ORC_OK;
+}
+
+/* ---------------------------------------------------------------- Philox4x32-10 */
+/* One Philox4x32 round: two 32x32->64 products of counter words 0 and 2 by the round
+ * multipliers; the new counter is (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1,
+ * lo(M0*c0)). Ten rounds, the key advanced by the Weyl constants between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint64_t p0 = (uint64_t)M0 * c0;
+    const uint64_t p1 = (uint64_t)M1 * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n1 = (uint32_t)p1;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    const uint32_t n3 = (uint32_t)p0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The 32 random bits of element i of a row with this seed and offset: word i % 4 of
+ * Philox4x32-10 at counter (i/4 low 32 bits, i/4 high 32 bits, offset low, offset high),
+ * key (seed low, seed high). */
+uint32_t oracle_philox_bits(uint64_t seed, uint64_t offset, uint64_t i) {
+  const uint64_t g = i >> 2;
+  const uint32_t ctr[4] = {(uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset,
+                           (uint32_t)(offset >> 32)};
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  return out[i & 3];
+}
+
+/* Uniform in (0, 1) from 32 random bits: the top 23 bits k give u = (2k + 1) / 2^24, the
+ * midpoints of 2^23 equal cells (exactly representable in binary32, never 0 or 1). */
+double oracle_uniform(uint32_t bits) {
+  return (double)(2u * (bits >> 9) + 1u) / 16777216.0;
+}
+
+/* Score of element i: logits/T + G with G = -ln(-ln u); T <= 0 (greedy) gives the logit
+ * alone. A NaN logit scores -inf. */
+static double gumbel_score(double logit, double temperature, uint64_t seed, uint64_t offset,
+                           uint64_t i) {
+  if (isnan(logit)) return -INFINITY;
+  if (!(temperature > 0.0)) return logit;
+  const double u = oracle_uniform(oracle_philox_bits(seed, offset, i));
+  return logit / temperature - log(-log(u));
+}
+
+/* Gumbel-max sample of every row: the index of the largest score, the lowest index among
+ * equal scores (a row of -inf scores gives 0). logits: row-major with row_stride elements
+ * between rows, binary32 (is_bf16 = 0) or bf16 bits (is_bf16 = 1). Writes the index, the
+ * largest score and the second largest (gap to the runner-up) per row. */
+int oracle_gumbel_sample(int64_t* out, double* best, double* second, const void* logits,
+                         int64_t row_stride, int is_bf16, int num_rows, int64_t vocab,
+                         const float* temperatures, const uint64_t* seeds,
+                         const uint64_t* offsets, int nthreads) {
+  if (num_rows < 0 || vocab <= 0 || row_stride < vocab) return ORC_BAD_SHAPE;
+  set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int b = 0; b < num_rows; ++b) {
+    double m1 = -INFINITY, m2 = -INFINITY;
+    int64_t arg = 0;
+    for (int64_t i = 0; i < vocab; ++i) {
+      double l;
+      if (is_bf16) {
+        l = bf16_bits_to_double(((const uint16_t*)logits)[(int64_t)b * row_stride + i]);
+      } else {
+        l = (double)((const float*)logits)[(int64_t)b * row_stride + i];
+      }
+      const double x = gumbel_score(l, (double)temperatures[b], seeds[b], offsets[b], i);
+      if (x > m1) {
+        m2 = m1;
+        m1 = x;
+        arg = i;
+      } else if (x > m2) {
+        m2 = x;
+      }
+    }
+    out[b] = arg;
+    if (best) best[b] = m1;
+    if (second) second[b] = m2;
+  }
+  return ORC_OK;
+}
+
+/* Every score of one row (for tests that check a choice among near-equal scores). */
+int oracle_gumbel_scores(double* scores, const void* logits, int is_bf16, int64_t vocab,
+                         float temperature, uint64_t seed, uint64_t offset) {
+  for (int64_t i = 0; i < vocab; ++i) {
+    const double l = is_bf16 ? bf16_bits_to_double(((const uint16_t*)logits)[i])
+                             : (double)((const float*)logits)[i];
+    scores[i] = gumbel_score(l, (double)temperature, seed, offset, i);
   }
   return ORC_OK;
 }

@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_sampler_oracle_cpu as gs
 from tests import test_staged_write_cpu as sw
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -45,6 +46,21 @@ MUTANTS = [
      [sw.test_oracle_reproduces_the_pages_usage_example]),
     ("staged_values_not_advanced", "taken += w_len[w];", "taken += 0;",
      [sw.test_oracle_later_write_wins_on_overlap]),
+    ("gumbel_is_exponential", "return logit / temperature - log(-log(u));",
+     "return logit / temperature - log(u);",
+     [gs.test_samples_follow_softmax_over_seeds]),
+    ("gumbel_times_temperature", "return logit / temperature - log(-log(u));",
+     "return logit * temperature - log(-log(u));",
+     [gs.test_samples_follow_softmax_over_seeds]),
+    ("philox_no_key_bump", "      k0 += W0;\n", "      k0 += 0;\n",
+     [gs.test_philox_known_answer_vectors]),
+    ("philox_swapped_product_word", "const uint32_t n1 = (uint32_t)p1;",
+     "const uint32_t n1 = (uint32_t)(p1 >> 32);",
+     [gs.test_philox_known_answer_vectors]),
+    ("uniform_wrong_shift", "(2u * (bits >> 9) + 1u)", "(2u * (bits >> 8) + 1u)",
+     [gs.test_uniform_mapping_closed_form]),
+    ("ties_to_highest_index", "      if (x > m1) {", "      if (x >= m1) {",
+     [gs.test_greedy_is_numpy_argmax_with_lowest_index_on_ties]),
 ]
 
 
@@ -57,6 +73,8 @@ def _call(fn):
         return fn(True)
     if "bs" in params:
         return fn(4)
+    if "T" in params:
+        return fn(0.7)
     if "dtype" in params:
         import numpy as np
         return fn(np.int32)
