@@ -62,6 +62,24 @@ DECODE_SOURCES = ("decode_kernel.cuh", "pa_device.cuh")
 PREFILL_SOURCES = ("prefill.cu", "umma.cuh", "pa_device.cuh")
 
 
+def profile_value(sources, summary: str, key: str):
+    """A number recorded as `key: value` in a committed ncu summary, if the summary was
+    taken on the current kernel sources (sha256 recorded in it); otherwise None."""
+    path = os.path.join(ROOT, "profiles", summary)
+    try:
+        text = open(path).read()
+        m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        m_v = re.search(re.escape(key) + r":\s*([0-9.eE+]+)", text)
+        if m_sha and m_v and m_sha.group(1) == source_sha256(*sources):
+            return float(m_v.group(1))
+    except OSError:
+        pass
+    return None
+
+
+SAMPLER_SOURCES = ("sample.cu", "pa_device.cuh")
+
+
 def kernel_traffic(sources, summary: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
     kernel sources (sha256 recorded in the summary); otherwise None."""
@@ -373,6 +391,73 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None):
             "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
 
 
+def measure_sampler(dev, steps: int, warmup: int):
+    """Gumbel-max sampling of one token per row: B=256 rows of the Qwen3 vocabulary
+    (V=151936), fp32 logits N(0, 9), T ~ U[0.3, 1.5], random seeds and offsets. The
+    logits rotate over buffers totalling more than L2, so every launch reads from HBM.
+    Bytes per launch = the logits read (B*V*4) plus the small per-row inputs/outputs."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_107_gb300 as pk
+
+    B, V = 256, 151936
+    rng = np.random.default_rng(107300)
+    temps = torch.from_numpy(rng.uniform(0.3, 1.5, size=B).astype(np.float32)).to(dev)
+    seeds = torch.from_numpy(rng.integers(0, 2**63, size=B, dtype=np.int64)).to(dev)
+    offs = torch.from_numpy(rng.integers(0, 2**40, size=B, dtype=np.int64)).to(dev)
+    out = torch.empty(B, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pk.SampleWorkspace(B, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, _, peak_src = measured_peaks()
+    res = {"workload": "gumbel_sample_b256_v151936", "num_seqs": B, "vocab": V,
+           "peak_gbs": hbm_peak, "peak_source": f"{peak_src} HBM copy GB/s"}
+    for dtype, name, nbuf in ((torch.float32, "fp32", 3), (torch.bfloat16, "bf16", 5)):
+        g = torch.Generator(device=dev)
+        g.manual_seed(107300)
+        bufs = [(torch.randn((B, V), generator=g, device=dev) * 3).to(dtype) for _ in range(nbuf)]
+
+        def launch(i):
+            pk.pa_gumbel_sample(out, bufs[i % nbuf], temps, seeds, offs, workspace=ws,
+                                dev_err=err, stream=stream)
+
+        for i in range(max(warmup, 3)):
+            launch(i)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            launch(i)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        nbytes = B * V * bufs[0].element_size() + B * (4 + 8 + 8 + 8)
+        res[name] = {"kernel_us": ms * 1e3, "bytes_per_launch": nbytes,
+                     "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                     "tokens_per_s": B / (ms * 1e-3)}
+        if name == "fp32":
+            # bound by instruction issue: warp instructions per launch (committed ncu
+            # capture of the same sources) over the live time, against one warp
+            # instruction per scheduler per cycle at the maximum SM clock
+            inst = profile_value(SAMPLER_SOURCES, "gumbel_sample_b256_v151936.md",
+                                 "inst_executed_per_launch")
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            peak = sms * 4 * 2.07e9
+            res[name]["roofline"] = {
+                "bound": "alu", "unit": "warp instructions/s", "peak": peak,
+                "peak_source": f"{sms} SMs x 4 schedulers x 1 instruction/cycle x 2.07 GHz",
+                "achieved": inst / (ms * 1e-3) if inst else None,
+                "frac": inst / (ms * 1e-3) / peak if inst else None,
+                "inst_per_launch": inst}
+        del bufs
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} in the sampler")
+    return res
+
+
 def measure_staged(dev, steps: int, warmup: int):
     """Block-table update through StagedWriteTensor ("Model Runner V2 设计文档", section 4):
     a [1024, 1000] int32 table on the device; each step appends one block id to 256
@@ -611,6 +696,7 @@ def run_ours(args):
     if not args.no_prefill:
         line["prefill"] = measure_prefill(dev, steps=min(args.steps, 20), warmup=args.warmup)
         line["staged_write"] = measure_staged(dev, steps=min(args.steps, 50), warmup=args.warmup)
+        line["sampler"] = measure_sampler(dev, steps=min(args.steps, 50), warmup=args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(case, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["gbs"], "unit": "GB/s", "cores": cb["cores"],
@@ -637,11 +723,20 @@ def main():
                     help="skip the secondary chunked-prefill measurement")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill step (for profiler captures)")
+    ap.add_argument("--sampler-only", action="store_true",
+                    help="time only the Gumbel-max sampler (for profiler captures)")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="override the block pool size (a smaller pool for profiler captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sampler_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_sampler(dev, args.steps, args.warmup)))
     elif args.prefill_only:
         import torch
         import paged_kv_cache_107_gb300 as pk

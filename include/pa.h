@@ -67,6 +67,9 @@ enum pa_dev_error {
   PA_DEV_ERR_STAGED = 32   /* a staged run outside the tensor, or run offsets that decrease */
 };
 
+/* Element types of inputs that are not always bf16 (the sampler's logits). */
+enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 };
+
 /* Human-readable name of a pa_status value. Never NULL. */
 const char* pa_status_str(int status);
 
@@ -168,6 +171,41 @@ int pa_staged_pack(const int32_t* rows, const int32_t* starts, const int32_t* le
 int pa_staged_upload_apply(void* base, int64_t num_rows, int64_t num_cols, int64_t row_stride,
                            int elem_bytes, const void* packed_host, void* packed_dev,
                            const pa_staged_layout* layout, int* dev_err, void* stream);
+
+/*
+ * pa_sample_workspace_size — bytes of scratch pa_gumbel_sample needs for num_seqs rows
+ * (0 for num_seqs < 0).
+ *
+ * pa_gumbel_sample — one token per row of logits, drawn from softmax(logits / T) by the
+ * Gumbel-max trick, without materialising the softmax.
+ * Source: "nano-vllm解读", section "Gumbel-Max采样" (argmax_i (ln p_i + G_i),
+ * G_i = -ln(-ln u_i), u_i ~ U(0,1) independent, has the law p); "Model Runner V2 设计文档",
+ * section 6 "Gumbel 采样内核" (no softmax materialised; stateless in-kernel random numbers
+ * from a seed input).
+ *
+ *   out             device, int64 [num_seqs]: the sampled index of each row.
+ *   logits          device, [num_seqs, row_stride] of binary32 (PA_DTYPE_F32) or bf16
+ *                   (PA_DTYPE_BF16); columns 0..vocab_size-1 are the logits.
+ *   temperatures    device, fp32 [num_seqs]; T <= 0 (or NaN) samples greedily.
+ *   seeds, offsets  device, uint64 [num_seqs]: the generator's key and stream position for
+ *                   the row (for example a request's seed and its decode step).
+ *   workspace       device, >= pa_sample_workspace_size(num_seqs) bytes, 256-byte aligned,
+ *                   ZERO before the first call; every call leaves it zero again. Calls
+ *                   that overlap in time need different workspaces.
+ *
+ * Definition (bit-reproducible across calls and launch shapes): element i of row b draws
+ * the 32-bit word i % 4 of Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy
+ * as 1, 2, 3", SC 2011) at counter (i/4 mod 2^32, i/2^34, offset mod 2^32, offset/2^32)
+ * under key (seed mod 2^32, seed/2^32); k = that word >> 9 gives u = (2k + 1) / 2^24. The
+ * score is logits[i] / T - ln(-ln u) in fp32 (the logit alone when T <= 0); a NaN score
+ * never wins; the largest score wins, the lowest index among equal scores; a row whose
+ * scores are all -inf or NaN gives 0.
+ */
+size_t pa_sample_workspace_size(int num_seqs);
+int pa_gumbel_sample(int64_t* out, const void* logits, int64_t row_stride, int logits_dtype,
+                     int num_seqs, int vocab_size, const float* temperatures,
+                     const uint64_t* seeds, const uint64_t* offsets, void* workspace,
+                     size_t workspace_bytes, int* dev_err, void* stream);
 
 /*
  * pa_decode_workspace_size — bytes of scratch that pa_decode needs for num_seqs

@@ -21,7 +21,8 @@ from . import build as _build
 __all__ = ["pa_store_kvcache", "pa_decode", "pa_decode_step", "pa_decode_workspace_size",
            "pa_prefill_varlen", "pa_decode_noalloc", "pa_staged_write_apply",
            "pa_staged_pack", "pa_staged_pack_bound", "pa_staged_upload_apply",
-           "PaStagedLayout",
+           "PaStagedLayout", "pa_sample_workspace_size", "pa_gumbel_sample",
+           "SampleWorkspace",
            "pa_status_str", "pa_version", "DecodeWorkspace", "library_path", "load_library",
            "PA_DEV_ERR"]
 
@@ -71,6 +72,10 @@ def load_library(path: Optional[str] = None):
         lib.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, i32, vp, i32,
                                        i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp]
         lib.pa_decode_step.restype = i32
+        lib.pa_sample_workspace_size.argtypes = [i32]
+        lib.pa_sample_workspace_size.restype = sz
+        lib.pa_gumbel_sample.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, vp, sz, vp, vp]
+        lib.pa_gumbel_sample.restype = i32
         lib.pa_staged_write_apply.argtypes = [vp, i64, i64, i64, i32, vp, vp, vp, vp, i32, i64,
                                               vp, vp]
         lib.pa_staged_write_apply.restype = i32
@@ -224,6 +229,56 @@ def pa_staged_upload_apply(base: torch.Tensor, packed_host: torch.Tensor,
             packed_host.data_ptr(), packed_dev.data_ptr(), ctypes.byref(layout),
             _ptr(dev_err), _stream(stream))
     _check(rc, "pa_staged_upload_apply")
+
+
+PA_DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def pa_sample_workspace_size(num_seqs: int) -> int:
+    return int(load_library().pa_sample_workspace_size(num_seqs))
+
+
+class SampleWorkspace:
+    """Zero-initialised sampler scratch (per-row keys and arrival counters; every call
+    leaves it zero). One workspace per stream of concurrent calls."""
+
+    def __init__(self, num_seqs: int, device=None):
+        self.nbytes = pa_sample_workspace_size(max(num_seqs, 1))
+        self.num_seqs = num_seqs
+        self.buffer = torch.zeros(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+_sample_ws = {}
+
+
+def pa_gumbel_sample(out: torch.Tensor, logits: torch.Tensor, temperatures: torch.Tensor,
+                     seeds: torch.Tensor, offsets: torch.Tensor,
+                     workspace: Optional[SampleWorkspace] = None,
+                     dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out int64 [B]; logits [B, V] fp32 or bf16 with contiguous columns (any row stride);
+    temperatures fp32 [B] (<= 0: greedy); seeds, offsets int64 [B] read as uint64."""
+    if logits.dim() != 2 or logits.stride(1) != 1 or logits.dtype not in PA_DTYPE:
+        raise PagedAttentionError("logits must be 2-D fp32/bf16 with contiguous columns")
+    if not logits.is_cuda:
+        raise PagedAttentionError("logits must be a CUDA tensor")
+    B, V = logits.shape
+    _need(out, "out", torch.int64, 1)
+    _need(temperatures, "temperatures", torch.float32, 1)
+    _need(seeds, "seeds", torch.int64, 1)
+    _need(offsets, "offsets", torch.int64, 1)
+    if not (out.shape[0] == temperatures.shape[0] == seeds.shape[0] == offsets.shape[0] == B):
+        raise PagedAttentionError("out / temperatures / seeds / offsets must have B entries")
+    if workspace is None:
+        key = (logits.device.index, B)
+        workspace = _sample_ws.get(key)
+        if workspace is None:
+            workspace = _sample_ws[key] = SampleWorkspace(B, device=logits.device)
+    rc = load_library().pa_gumbel_sample(
+        _ptr(out), _ptr(logits), logits.stride(0) if B > 1 else V, PA_DTYPE[logits.dtype], B, V,
+        _ptr(temperatures), _ptr(seeds), _ptr(offsets), _ptr(workspace.buffer),
+        workspace.nbytes, _ptr(dev_err), _stream(stream))
+    _check(rc, "pa_gumbel_sample")
+    return out
 
 
 def pa_decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,

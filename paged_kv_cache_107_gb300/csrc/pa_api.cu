@@ -126,6 +126,33 @@ int pa_staged_upload_apply(void* base, int64_t num_rows, int64_t num_cols, int64
                                         static_cast<cudaStream_t>(stream), info.num_sms);
 }
 
+size_t pa_sample_workspace_size(int num_seqs) {
+  if (num_seqs < 0) return 0;
+  return pa::sample_workspace_bytes(num_seqs > 0 ? num_seqs : 1);
+}
+
+int pa_gumbel_sample(int64_t* out, const void* logits, int64_t row_stride, int logits_dtype,
+                     int num_seqs, int vocab_size, const float* temperatures,
+                     const uint64_t* seeds, const uint64_t* offsets, void* workspace,
+                     size_t workspace_bytes, int* dev_err, void* stream) {
+  if (num_seqs < 0 || vocab_size <= 0 || row_stride < vocab_size) return PA_ERR_SHAPE;
+  if (logits_dtype != PA_DTYPE_F32 && logits_dtype != PA_DTYPE_BF16) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !logits || !temperatures || !seeds || !offsets) return PA_ERR_NULL;
+  if (!workspace || workspace_bytes < pa::sample_workspace_bytes(num_seqs))
+    return PA_ERR_WORKSPACE;
+  const uintptr_t esz = logits_dtype == PA_DTYPE_BF16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(logits) % esz) || (reinterpret_cast<uintptr_t>(out) & 7) ||
+      (reinterpret_cast<uintptr_t>(seeds) & 7) || (reinterpret_cast<uintptr_t>(offsets) & 7) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return PA_ERR_ALIGN;
+  pa::DeviceInfo info;
+  if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
+  return pa::launch_gumbel_sample(out, logits, row_stride, logits_dtype == PA_DTYPE_BF16,
+                                  num_seqs, vocab_size, temperatures, seeds, offsets, workspace,
+                                  dev_err, static_cast<cudaStream_t>(stream), info.num_sms);
+}
+
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim != pa::kHeadDimApi)
     return 0;

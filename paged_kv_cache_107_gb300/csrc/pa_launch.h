@@ -39,6 +39,12 @@ int launch_staged_upload_apply(void* base, int64_t num_rows, int64_t num_cols,
                                void* packed_dev, const pa_staged_layout* lay, int* dev_err,
                                cudaStream_t stream, int num_sms);
 
+size_t sample_workspace_bytes(int num_rows);
+int launch_gumbel_sample(int64_t* out, const void* logits, int64_t row_stride, int is_bf16,
+                         int num_rows, int vocab, const float* temperatures,
+                         const uint64_t* seeds, const uint64_t* offsets, void* workspace,
+                         int* dev_err, cudaStream_t stream, int num_sms);
+
 struct DecodeArgs {
   void* out;
   const void* q;

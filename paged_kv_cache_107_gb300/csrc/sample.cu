@@ -1,0 +1,487 @@
+// sample.cu — Gumbel-max sampling of one token per row of logits [B, V].
+//
+// "nano-vllm解读", section "Gumbel-Max采样": sampling from softmax(logits / T) equals taking
+// argmax_i (ln p_i + G_i) with G_i = -ln(-ln u_i), u_i independent U(0,1); ln p_i and
+// logits_i / T differ by a constant of the row, so the score is logits_i / T + G_i.
+// "Model Runner V2 设计文档", section 6 ("Gumbel 采样内核"): no softmax is materialised and
+// the random numbers come from a stateless in-kernel generator keyed by a seed input.
+//
+// Generator: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC 2011). Element i of a row draws word i % 4 of the block at counter
+// (i / 4, i / 2^34, offset lo, offset hi) under key (seed lo, seed hi); u = (2k + 1) / 2^24
+// from the top 23 bits k (exact in binary32, never 0 or 1). T <= 0 samples greedily (the
+// logit alone), a NaN logit never wins, ties go to the lowest index. The kernels rank by
+// log2(e) * score - log2(log2(e)), which orders the elements exactly as the score does.
+//
+// Design (the logits are read once; the arithmetic is one Philox block per 4 elements and
+// two or three special-function operations per element):
+//  * Rows that start on 16 bytes: a persistent CTA per SM takes an even share of the
+//    (row, 32 KB tile) stream. A producer warp moves tiles with cp.async.bulk into a
+//    4-stage shared-memory ring (mbarrier full/empty pairs, bounded waits); consumer
+//    warps score them from shared memory, one 16-byte group per thread at a time.
+//  * Other rows: one CTA per (row, 8192-element chunk) with plain loads.
+//  * The running best is a 64-bit key: order-preserving bits of the score in the high
+//    word, ~index in the low word, so an unsigned max picks the largest score and, among
+//    equal scores, the lowest index. When a CTA leaves a row it reduces its key (warps,
+//    then one thread), does one atomicMax into the row's key and adds its tile count to the
+//    row's arrival counter; the CTA that completes the count writes the index and resets
+//    key and counter to zero for the next call. One launch, deterministic.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_device.cuh"
+#include "pa_launch.h"
+
+namespace pa {
+namespace {
+
+constexpr int kSampleThreads = 256;
+constexpr int kSampleChunk = 8192;  // elements per CTA of the plain-load kernel
+#ifndef PA_SAMPLE_RING_WARPS
+#define PA_SAMPLE_RING_WARPS 16
+#endif
+constexpr int kSampleRingWarps = PA_SAMPLE_RING_WARPS;  // consumer warps of the ring kernel
+
+__device__ __forceinline__ void philox4x32_10(uint32_t& c0, uint32_t& c1, uint32_t& c2,
+                                              uint32_t& c3, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    uint64_t p0, p1;  // full 32x32 -> 64-bit products
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(M0), "r"(c0));
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(M1), "r"(c2));
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c0 = n0;
+    c1 = (uint32_t)p1;
+    c2 = n2;
+    c3 = (uint32_t)p0;
+    k0 += W0;
+    k1 += W1;
+  }
+}
+
+// -log2(u) for u = (2k + 1) / 2^24, k the top 23 bits of `bits`, with relative accuracy
+// over the whole range. u = (1 + k/2^23) - (1 - 2^-24) and w = 1 - u =
+// (1 + (2^23 - 1 - k)/2^23) - (1 - 2^-24) are both exact in binary32. For u < 1/2 the
+// hardware log2 (|log2 u| >= 1, so its absolute error is a small relative one); for
+// u >= 1/2, -log2(1 - w) = (2 / ln 2) atanh(s) with s = w / (2 - w) <= 1/3, summed by the
+// Taylor series of atanh up to s^11 (truncation below 1.5e-7 relative).
+__device__ __forceinline__ float neg_log2_uniform(uint32_t bits) {
+  const uint32_t k = bits >> 9;
+  const float u = __uint_as_float(0x3F800000u | k) - 0.99999994039535522f;
+  const float w = __uint_as_float(0x3F800000u | (k ^ 0x7FFFFFu)) - 0.99999994039535522f;
+  const float a = -fast_log2(u);
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(2.f - w));
+  const float s = w * r;
+  const float s2 = s * s;
+  float p = 0.26230818925253880f;         // (2 / ln 2) / 11
+  p = fmaf(p, s2, 0.32059889797532520f);  // (2 / ln 2) / 9
+  p = fmaf(p, s2, 0.41219858311113240f);  // (2 / ln 2) / 7
+  p = fmaf(p, s2, 0.57707801635558540f);  // (2 / ln 2) / 5
+  p = fmaf(p, s2, 0.96179669392597560f);  // (2 / ln 2) / 3
+  p = fmaf(p, s2, 2.88539008177792680f);  // 2 / ln 2
+  return k < (1u << 22) ? a : s * p;
+}
+
+// Ranking score of one element in log2 units: l * (log2(e) / T) - log2(-log2 u).
+__device__ __forceinline__ float rank_score(float l, float scale, uint32_t bits) {
+  return fmaf(l, scale, -fast_log2(neg_log2_uniform(bits)));
+}
+
+__device__ __forceinline__ uint64_t score_key(float x, int64_t i) {
+  uint32_t b = __float_as_uint(x);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)b << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i);
+}
+
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+struct SampleArgs {
+  const void* logits;
+  int64_t row_stride;
+  int vocab;
+  int num_rows;
+  int chunks;
+  const float* temperatures;
+  const uint64_t* seeds;
+  const uint64_t* offsets;
+  int64_t* out;
+  unsigned long long* keys;  // [num_rows], zero between calls
+  int* counters;             // [num_rows], zero between calls
+  int* dev_err;
+};
+
+// T: float (4 elements per 16-byte group) or uint16_t bf16 bits (8 per group).
+// Key of a CTA's best: reduce over the consumer threads (warp shuffles, then one thread
+// over the warps' keys in `slots`; `sync` is the barrier over those threads), then one
+// atomicMax into the row's key and `tiles` added to its arrival counter. The thread that
+// completes the count (tiles of the row = chunks) writes the index and zeroes both.
+template <typename Sync>
+__device__ __forceinline__ void flush_row(const SampleArgs& a, int row, int tiles, float best_x,
+                                          int64_t best_i, uint64_t* slots, int nwarps,
+                                          int ctid, Sync sync) {
+  uint64_t key = score_key(best_x, best_i);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, m));
+  if ((ctid & 31) == 0) slots[ctid >> 5] = key;
+  sync();
+  if (ctid == 0) {
+    uint64_t k = slots[0];
+    for (int w = 1; w < nwarps; ++w) k = umax64(k, slots[w]);
+    atomicMax(a.keys + row, (unsigned long long)k);
+    __threadfence();
+    const int before = atomicAdd(a.counters + row, tiles);
+    if (before + tiles == a.chunks) {
+      __threadfence();
+      const unsigned long long fin = atomicExch(a.keys + row, 0ull);
+      a.out[row] = (int64_t)(0xFFFFFFFFu - (uint32_t)(fin & 0xFFFFFFFFull));
+      a.counters[row] = 0;
+    }
+  }
+}
+
+__device__ __forceinline__ float widen(float v) { return v; }
+__device__ __forceinline__ float widen(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+
+// Score the n (<= 4) elements i0.. of a Philox block (i0 a multiple of 4) and keep the best.
+__device__ __forceinline__ void score_block(const float* l, int64_t i0, int n, bool greedy,
+                                           float scale, uint32_t k0, uint32_t k1, uint32_t o0,
+                                           uint32_t o1, float& best_x, int64_t& best_i) {
+  uint32_t r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+  if (!greedy) {
+    const uint64_t g = (uint64_t)i0 >> 2;
+    r0 = (uint32_t)g;
+    r1 = (uint32_t)(g >> 32);
+    r2 = o0;
+    r3 = o1;
+    philox4x32_10(r0, r1, r2, r3, k0, k1);
+  }
+  const uint32_t rw[4] = {r0, r1, r2, r3};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (e < n) {
+      const float x = greedy ? l[e] : rank_score(l[e], scale, rw[e]);
+      if (x > best_x) {  // NaN never passes; equal scores keep the earlier index
+        best_x = x;
+        best_i = i0 + e;
+      }
+    }
+  }
+}
+
+// Rows that do not start on 16 bytes: one CTA per (row, chunk of kSampleChunk elements),
+// plain loads of 4 consecutive elements per thread at a time.
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads) gumbel_sample_chunk_kernel(const SampleArgs a) {
+  const int b = blockIdx.x / a.chunks;
+  const int chunk = blockIdx.x - b * a.chunks;
+  const int64_t c_begin = (int64_t)chunk * kSampleChunk;
+  const int64_t c_end = min((int64_t)a.vocab, c_begin + kSampleChunk);
+  const T* row = static_cast<const T*>(a.logits) + (int64_t)b * a.row_stride;
+  const float temp = __ldg(a.temperatures + b);
+  const bool greedy = !(temp > 0.f);
+  const float scale = greedy ? 1.f : 1.4426950408889634f / temp;  // log2(e) / T
+  const uint64_t seed = __ldg(reinterpret_cast<const unsigned long long*>(a.seeds) + b);
+  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(a.offsets) + b);
+  float best_x = -INFINITY;
+  int64_t best_i = c_begin + (int64_t)threadIdx.x * 4;  // all -inf / NaN: the first element
+  for (int64_t q = c_begin + (int64_t)threadIdx.x * 4; q < c_end; q += 4 * kSampleThreads) {
+    float l[4];
+    const int n = (int)min((int64_t)4, c_end - q);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) l[e] = e < n ? widen(row[q + e]) : 0.f;
+    score_block(l, q, n, greedy, scale, (uint32_t)seed, (uint32_t)(seed >> 32), (uint32_t)off,
+                (uint32_t)(off >> 32), best_x, best_i);
+  }
+  __shared__ uint64_t slots[kSampleThreads / 32];
+  flush_row(a, b, 1, best_x, best_i, slots, kSampleThreads / 32, threadIdx.x,
+            [] { __syncthreads(); });
+}
+
+// ---------------------------------------------------------------- ring kernel
+constexpr int kRingStages = 4;
+constexpr int kTileBytes = 32768;
+
+struct RingCtrl {
+  uint64_t full[kRingStages];
+  uint64_t empty[kRingStages];
+  uint64_t slots[2][16];
+  int abort;
+};
+
+// Rows that start on 16 bytes: persistent CTAs over the (row, tile) stream, tiles moved
+// into shared memory by a producer warp, CW consumer warps.
+template <typename T, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(const SampleArgs a) {
+  constexpr int EPG = 16 / sizeof(T);            // elements per 16-byte group
+  constexpr int TE = kTileBytes / sizeof(T);     // elements per tile
+  constexpr int CT = CW * 32;                    // consumer threads
+  constexpr int GPT = kTileBytes / 16 / CT;      // groups per consumer thread per tile
+  static_assert(GPT * CT * 16 == kTileBytes, "tile split");
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  RingCtrl& ctl = *reinterpret_cast<RingCtrl*>(smem + kRingStages * kTileBytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int64_t nt = (int64_t)a.num_rows * a.chunks;
+  const int64_t x0 = (int64_t)blockIdx.x * nt / gridDim.x;
+  const int64_t x1 = (int64_t)(blockIdx.x + 1) * nt / gridDim.x;
+  if (x0 >= x1) return;  // no tiles: nothing initialised, nothing in flight
+  if (tid == 0) {
+    for (int st = 0; st < kRingStages; ++st) {
+      mbar_init(&ctl.full[st], 1);
+      mbar_init(&ctl.empty[st], CW);
+    }
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t n_tiles = x1 - x0;
+  volatile int* abort_flag = &ctl.abort;
+
+  if (warp == CW) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t policy = policy_evict_first();
+      for (int64_t it = 0; it < n_tiles; ++it) {
+        const int64_t x = x0 + it;
+        const int b = (int)(x / a.chunks);
+        const int64_t start = (x - (int64_t)b * a.chunks) * TE;
+        const int64_t n = min((int64_t)TE, (int64_t)a.vocab - start);
+        const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(T)) & ~15u;
+        const int st = (int)(it % kRingStages);
+        if (it >= kRingStages &&
+            !mbar_wait(&ctl.empty[st], (uint32_t)(((it / kRingStages) - 1) & 1), abort_flag)) {
+          ctl.abort = 1;
+          set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+        }
+        mbar_arrive_expect_tx(&ctl.full[st], bytes);
+        if (bytes)
+          bulk_g2s_hint(smem + (size_t)st * kTileBytes,
+                        static_cast<const T*>(a.logits) + (int64_t)b * a.row_stride + start, bytes,
+                        &ctl.full[st], policy);
+      }
+      // the last stages must land before the CTA may exit
+      const int64_t first = n_tiles > kRingStages ? n_tiles - kRingStages : 0;
+      for (int64_t it = first; it < n_tiles; ++it)
+        mbar_wait(&ctl.full[it % kRingStages], (uint32_t)((it / kRingStages) & 1), abort_flag);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  int cur = -1, row_tiles = 0, parity = 0;
+  float best_x = -INFINITY, scale = 1.f;
+  int64_t best_i = 0;
+  bool greedy = true;
+  uint32_t k0 = 0, k1 = 0, o0 = 0, o1 = 0;
+  uint32_t rk0[10], rk1[10];  // Philox round keys of the current row
+  auto sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory"); };
+  for (int64_t it = 0; it < n_tiles; ++it) {
+    const int64_t x = x0 + it;
+    const int b = (int)(x / a.chunks);
+    const int64_t start = (x - (int64_t)b * a.chunks) * TE;
+    const int64_t n = min((int64_t)TE, (int64_t)a.vocab - start);
+    const int64_t n_bulk = ((n * (int64_t)sizeof(T)) & ~int64_t(15)) / (int64_t)sizeof(T);
+    if (b != cur) {
+      if (cur >= 0) {
+        flush_row(a, cur, row_tiles, best_x, best_i, ctl.slots[parity], CW, tid, sync);
+        parity ^= 1;
+      }
+      cur = b;
+      row_tiles = 0;
+      const float temp = __ldg(a.temperatures + b);
+      greedy = !(temp > 0.f);
+      scale = greedy ? 1.f : 1.4426950408889634f / temp;  // log2(e) / T
+      const uint64_t seed = __ldg(reinterpret_cast<const unsigned long long*>(a.seeds) + b);
+      const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(a.offsets) + b);
+      k0 = (uint32_t)seed;
+      k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+      for (int r = 0; r < 10; ++r) {
+        rk0[r] = k0 + (uint32_t)r * 0x9E3779B9u;
+        rk1[r] = k1 + (uint32_t)r * 0xBB67AE85u;
+      }
+      o0 = (uint32_t)off;
+      o1 = (uint32_t)(off >> 32);
+      best_x = -INFINITY;
+      best_i = start + (int64_t)tid * EPG;  // all -inf / NaN: the row's first element
+    }
+    const int st = (int)(it % kRingStages);
+    if (!mbar_wait(&ctl.full[st], (uint32_t)((it / kRingStages) & 1), abort_flag)) {
+      if (lane == 0) {
+        ctl.abort = 1;
+        set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+      }
+    }
+    const unsigned char* tile = smem + (size_t)st * kTileBytes;
+    uint4 raw[GPT];
+#pragma unroll
+    for (int k = 0; k < GPT; ++k) raw[k] = lds128(tile + ((size_t)k * CT + tid) * 16);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.empty[st]);  // the tile is in registers
+    // scores of this thread's elements, in increasing index order; the tile's maximum is
+    // located (first index holding it) only when it beats the running best
+    constexpr int NE = GPT * EPG;
+    float xs[NE];
+    const int s0 = (int)start;
+    const int nb = (int)n_bulk;
+#pragma unroll
+    for (int k = 0; k < GPT; ++k) {
+      float l[EPG];
+      if constexpr (sizeof(T) == 4) {
+        l[0] = __uint_as_float(raw[k].x);
+        l[1] = __uint_as_float(raw[k].y);
+        l[2] = __uint_as_float(raw[k].z);
+        l[3] = __uint_as_float(raw[k].w);
+      } else {
+        const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          l[2 * q] = __uint_as_float(w4[q] << 16);
+          l[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < EPG; ++e) xs[k * EPG + e] = l[e];  // the noise is added below
+    }
+    if (!greedy) {
+      // the thread's Philox blocks advanced together, round by round (NB independent
+      // chains interleaved), then the noise of each element
+      constexpr int NB = NE / 4;
+      uint32_t c0[NB], c1[NB], c2[NB], c3[NB];
+#pragma unroll
+      for (int q = 0; q < NB; ++q) {
+        const int k = q / (EPG / 4), h = q % (EPG / 4);
+        c0[q] = (uint32_t)((s0 + (k * CT + tid) * EPG) >> 2) + h;
+        c1[q] = 0;
+        c2[q] = o0;
+        c3[q] = o1;
+      }
+#pragma unroll
+      for (int r = 0; r < 10; ++r) {
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+          uint64_t p0, p1;
+          asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(0xD2511F53u), "r"(c0[q]));
+          asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(0xCD9E8D57u), "r"(c2[q]));
+          const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1[q] ^ rk0[r];
+          const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3[q] ^ rk1[r];
+          c0[q] = n0;
+          c1[q] = (uint32_t)p1;
+          c2[q] = n2;
+          c3[q] = (uint32_t)p0;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NB; ++q) {
+        xs[4 * q + 0] = rank_score(xs[4 * q + 0], scale, c0[q]);
+        xs[4 * q + 1] = rank_score(xs[4 * q + 1], scale, c1[q]);
+        xs[4 * q + 2] = rank_score(xs[4 * q + 2], scale, c2[q]);
+        xs[4 * q + 3] = rank_score(xs[4 * q + 3], scale, c3[q]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < GPT; ++k)
+      if ((k * CT + tid) * EPG >= nb) {
+#pragma unroll
+        for (int e = 0; e < EPG; ++e) xs[k * EPG + e] = -INFINITY;  // past the bulk part
+      }
+    float m = xs[0];
+#pragma unroll
+    for (int j = 1; j < NE; ++j) m = fmaxf(m, xs[j]);  // NaN is skipped by fmaxf
+    if (m > best_x) {
+      int jj = 0;
+#pragma unroll
+      for (int j = NE - 1; j >= 0; --j)
+        if (xs[j] == m) jj = j;  // the first element holding the maximum
+      best_x = m;
+      best_i = s0 + ((jj / EPG) * CT + tid) * EPG + (jj % EPG);
+    }
+    // a ragged end of the row (fewer than 16 bytes): plain loads, one element per thread
+    if (tid < n - n_bulk) {
+      const int i = s0 + nb + tid;
+      const T* rowp = static_cast<const T*>(a.logits) + (int64_t)b * a.row_stride;
+      const float lv = widen(rowp[i]);
+      float xv = lv;
+      if (!greedy) {
+        uint32_t r0 = (uint32_t)(i >> 2), r1 = 0, r2 = o0, r3 = o1;
+        philox4x32_10(r0, r1, r2, r3, k0, k1);
+        const int e = i & 3;
+        xv = rank_score(lv, scale, e == 0 ? r0 : e == 1 ? r1 : e == 2 ? r2 : r3);
+      }
+      if (xv > best_x || (xv == best_x && i < best_i)) {
+        best_x = xv;
+        best_i = i;
+      }
+    }
+    ++row_tiles;
+  }
+  flush_row(a, cur, row_tiles, best_x, best_i, ctl.slots[parity], CW, tid, sync);
+}
+
+}  // namespace
+
+size_t sample_workspace_bytes(int num_rows) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return up((size_t)num_rows * 8) + up((size_t)num_rows * 4);
+}
+
+namespace {
+template <typename T, int CW>
+int launch_ring(const SampleArgs& a, cudaStream_t stream, int num_sms) {
+  const size_t smem = (size_t)kRingStages * kTileBytes + sizeof(RingCtrl) + 128;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(gumbel_sample_ring_kernel<T, CW>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  const int64_t nt = (int64_t)a.num_rows * a.chunks;
+  const int grid = (int)(nt < num_sms ? nt : num_sms);
+  gumbel_sample_ring_kernel<T, CW><<<grid, (CW + 1) * 32, smem, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+}  // namespace
+
+int launch_gumbel_sample(int64_t* out, const void* logits, int64_t row_stride, int is_bf16,
+                         int num_rows, int vocab, const float* temperatures,
+                         const uint64_t* seeds, const uint64_t* offsets, void* workspace,
+                         int* dev_err, cudaStream_t stream, int num_sms) {
+  SampleArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.vocab = vocab;
+  a.num_rows = num_rows;
+  a.temperatures = temperatures;
+  a.seeds = seeds;
+  a.offsets = offsets;
+  a.out = out;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.keys = reinterpret_cast<unsigned long long*>(ws);
+  a.counters = reinterpret_cast<int*>(ws + (((size_t)num_rows * 8 + 255) & ~size_t(255)));
+  a.dev_err = dev_err;
+  const int esz = is_bf16 ? 2 : 4;
+  const bool ring = (reinterpret_cast<uintptr_t>(logits) & 15) == 0 && ((row_stride * esz) & 15) == 0;
+  if (ring) {
+    a.chunks = (int)(((int64_t)vocab * esz + kTileBytes - 1) / kTileBytes);
+    return is_bf16 ? launch_ring<uint16_t, kSampleRingWarps>(a, stream, num_sms)
+                   : launch_ring<float, kSampleRingWarps>(a, stream, num_sms);
+  }
+  a.chunks = (vocab + kSampleChunk - 1) / kSampleChunk;
+  const int64_t grid = (int64_t)a.chunks * num_rows;
+  if (grid > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (is_bf16) gumbel_sample_chunk_kernel<uint16_t><<<(unsigned)grid, kSampleThreads, 0, stream>>>(a);
+  else gumbel_sample_chunk_kernel<float><<<(unsigned)grid, kSampleThreads, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa

@@ -85,6 +85,17 @@ def test_validation_without_launch(lib):
     assert step(1000, 128, 2) == 2
     assert step(1024, 64, 2) == 3
     assert step(1024, 128, 0) == 0
+    # sampler: row stride below the vocabulary, unknown dtype, zero rows
+    lib.pa_gumbel_sample.restype = ctypes.c_int
+    lib.pa_sample_workspace_size.restype = ctypes.c_size_t
+
+    def sample(stride, dtype, B):
+        return lib.pa_gumbel_sample(vp, vp, i64(stride), dtype, B, 100, vp, vp, vp, vp,
+                                    ctypes.c_size_t(1 << 20), None, None)
+    assert sample(99, 0, 4) == 2
+    assert sample(100, 7, 4) == 3
+    assert sample(100, 0, 0) == 0
+    assert lib.pa_sample_workspace_size(-1) == 0 and lib.pa_sample_workspace_size(256) >= 256 * 12
     # prefill: max_seqlen_k beyond what the table maps
     lib.pa_prefill_varlen.restype = ctypes.c_int
     rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 256,
