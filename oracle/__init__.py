@@ -52,10 +52,12 @@ def _load(path=None):
         lib.oracle_store_kvcache.argtypes = [p, p, i64, i64, p, p, p, i64, i32, i32, i64]
         lib.oracle_store_kvcache.restype = i32
         lib.oracle_decode.argtypes = [p, p, p, p, p, p, i32, p, i32, i32, i32, i32, i32, i64,
-                                      dbl, p, i64, i32]
+                                      dbl, p, i64, i32, i32]
         lib.oracle_decode.restype = i32
         lib.oracle_prefill.argtypes = [p, p, p, p, p, p, i32, p, p, i32, i32, i32, i32, i32,
-                                       i64, i32, dbl, p, i64, i32]
+                                       i64, i32, dbl, p, i64, i32, i32]
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_double.restype = dbl
         lib.oracle_prefill.restype = i32
         lib.oracle_slot_of.argtypes = [p, i32, i64, i32]
         lib.oracle_slot_of.restype = i64
@@ -105,6 +107,25 @@ def _u16(a) -> np.ndarray:
     return a
 
 
+def _bits(a):
+    """16-bit float data (torch bf16 / fp16, numpy float16, or raw uint16 bf16 bits) as a
+    C-contiguous uint16 array of its bits, and 1 if it is IEEE binary16, else 0."""
+    if hasattr(a, "view") and hasattr(a, "dtype") and "float16" in str(a.dtype) \
+            and "bfloat16" not in str(a.dtype):
+        if hasattr(a, "detach"):  # torch
+            import torch
+            a = a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        else:
+            a = np.ascontiguousarray(a).view(np.uint16)
+        return np.ascontiguousarray(a), 1
+    return _u16(a), 0
+
+
+def f16_to_double(bits: int) -> float:
+    """Exact value of an IEEE binary16 bit pattern."""
+    return float(_load().oracle_f16_to_double(bits))
+
+
 def _i32(a) -> np.ndarray:
     if hasattr(a, "cpu"):
         a = a.detach().cpu().numpy()
@@ -127,14 +148,15 @@ def max_threads(nthreads: int = 0) -> int:
 
 
 def store_kvcache(k, v, k_cache, v_cache, slot_mapping):
-    """Return (k_cache', v_cache') as uint16 arrays after the store of the new rows.
+    """Return (k_cache', v_cache') as uint16 arrays (the raw 16-bit elements) after the
+    store of the new rows: a bit copy, so bf16 and fp16 alike.
 
-    k, v: bf16 [N, Hk, D]; caches bf16 [nb, bs, Hk, D]; slot_mapping int32 [N].
+    k, v: [N, Hk, D]; caches [nb, bs, Hk, D]; slot_mapping int32 [N].
     The inputs are not modified.
     """
     lib = _load()
-    k, v = _u16(k), _u16(v)
-    kc, vc = _u16(k_cache).copy(), _u16(v_cache).copy()
+    k, v = _bits(k)[0], _bits(v)[0]
+    kc, vc = _bits(k_cache)[0].copy(), _bits(v_cache)[0].copy()
     slots = _i32(slot_mapping)
     n, hk, d = k.shape
     num_slots = kc.shape[0] * kc.shape[1]
@@ -152,8 +174,9 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, pairs=No
     indices, is given) and, if return_lse, the natural-log LSE per row.
     """
     lib = _load()
-    q = _u16(q)
-    kc, vc = _u16(k_cache), _u16(v_cache)
+    q, f16 = _bits(q)
+    (kc, fk), (vc, fv) = _bits(k_cache), _bits(v_cache)
+    assert f16 == fk == fv, "q, k_cache and v_cache must share one element type"
     bt, ctx = _i32(block_tables), _i32(context_lens)
     B, H, D = q.shape
     nb, bs, hk, d2 = kc.shape
@@ -172,18 +195,19 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, pairs=No
     maxb = bt.shape[1] if bt.ndim == 2 else 0
     rc = lib.oracle_decode(_ptr(out), _ptr(lse), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), maxb,
                            _ptr(ctx), B, H, hk, D, bs, nb, float(scale), pp, npairs,
-                           int(nthreads))
+                           int(nthreads), f16)
     _check(rc, "decode")
     return (out, lse) if return_lse else out
 
 
 def prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, causal=True,
             scale=None, rows=None, nthreads=0, return_lse=False):
-    """fp64 varlen prefill attention. q bf16 [sum n, H, D]. rows: optional list of
-    token_row*H + h indices (compact output)."""
+    """fp64 varlen prefill attention. q bf16 or fp16 [sum n, H, D] (caches of the same type).
+    rows: optional list of token_row*H + h indices (compact output)."""
     lib = _load()
-    q = _u16(q)
-    kc, vc = _u16(k_cache), _u16(v_cache)
+    q, f16 = _bits(q)
+    (kc, fk), (vc, fv) = _bits(k_cache), _bits(v_cache)
+    assert f16 == fk == fv, "q, k_cache and v_cache must share one element type"
     bt = _i32(block_tables)
     cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
     T, H, D = q.shape
@@ -203,7 +227,7 @@ def prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, causa
     maxb = bt.shape[1] if bt.ndim == 2 else 0
     rc = lib.oracle_prefill(_ptr(out), _ptr(lse), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), maxb,
                             _ptr(cq), _ptr(ck), S, H, hk, D, bs, nb, 1 if causal else 0,
-                            float(scale), rp, nrows, int(nthreads))
+                            float(scale), rp, nrows, int(nthreads), f16)
     _check(rc, "prefill")
     return (out, lse) if return_lse else out
 

@@ -37,7 +37,8 @@
  *     staged write copies its values into one row of the tensor from a start column; the
  *     writes take effect one after another, in the order they were staged.
  *
- * bf16 values arrive as raw uint16 bits; each is widened exactly to double.
+ * bf16 (or IEEE binary16) values arrive as raw uint16 bits; each is widened exactly to
+ * double.
  * Parity status: every function here is pinned by the CPU tests (closed forms,
  * invariants, textbook special cases, brute force); see the test suite.
  */
@@ -64,6 +65,25 @@ static double bf16_bits_to_double(uint16_t bits) {
   memcpy(&f, &u, sizeof f);
   return (double)f;
 }
+
+/* Exact widening of an IEEE 754 binary16 bit pattern to double: sign, 5-bit exponent
+ * (bias 15), 10-bit fraction; exponent 0 holds the subnormals m * 2^-24, exponent 31 the
+ * infinities and NaNs. */
+static double f16_bits_to_double(uint16_t bits) {
+  const int sign = bits >> 15, e = (bits >> 10) & 31, m = bits & 1023;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp((double)(1024 + m), e - 25);
+  return sign ? -v : v;
+}
+
+/* The element types of q, k and v: bf16 (is_fp16 = 0) or IEEE binary16 (is_fp16 = 1). */
+static double elem_to_double(uint16_t bits, int is_fp16) {
+  return is_fp16 ? f16_bits_to_double(bits) : bf16_bits_to_double(bits);
+}
+
+double oracle_f16_to_double(uint16_t bits) { return f16_bits_to_double(bits); }
 
 int oracle_version(void) { return 1; }
 
@@ -115,7 +135,8 @@ static int64_t physical_row(const int32_t* table, int max_blocks, int64_t t, int
 static int attend_row(double* o, double* lse, const double* qv, const uint16_t* k_cache,
                       const uint16_t* v_cache, const int32_t* table, int max_blocks,
                       int64_t num_keys, int num_kv_heads, int kv_head, int D, int block_size,
-                      int64_t num_blocks, double scale, double* scores /* num_keys scratch */) {
+                      int64_t num_blocks, double scale, double* scores /* num_keys scratch */,
+                      int is_fp16) {
   int64_t row_elems = (int64_t)num_kv_heads * D;
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (num_keys <= 0) {
@@ -128,7 +149,7 @@ static int attend_row(double* o, double* lse, const double* qv, const uint16_t* 
     if (r < 0) return ORC_BAD_BLOCK;
     const uint16_t* kt = k_cache + r * row_elems + (int64_t)kv_head * D;
     double dot = 0.0;
-    for (int d = 0; d < D; ++d) dot += qv[d] * bf16_bits_to_double(kt[d]);
+    for (int d = 0; d < D; ++d) dot += qv[d] * elem_to_double(kt[d], is_fp16);
     scores[t] = scale * dot;
   }
   /* softmax */
@@ -145,7 +166,7 @@ static int attend_row(double* o, double* lse, const double* qv, const uint16_t* 
     int64_t r = physical_row(table, max_blocks, t, block_size, num_blocks);
     const uint16_t* vt = v_cache + r * row_elems + (int64_t)kv_head * D;
     double p = scores[t] / l;
-    for (int d = 0; d < D; ++d) o[d] += p * bf16_bits_to_double(vt[d]);
+    for (int d = 0; d < D; ++d) o[d] += p * elem_to_double(vt[d], is_fp16);
   }
   if (lse) *lse = m + log(l);
   return ORC_OK;
@@ -173,7 +194,7 @@ int oracle_decode(double* out, double* lse, const uint16_t* q, const uint16_t* k
                   const uint16_t* v_cache, const int32_t* block_tables, int max_blocks,
                   const int32_t* context_lens, int B, int H, int Hk, int D, int block_size,
                   int64_t num_blocks, double scale, const int64_t* pairs, int64_t num_pairs,
-                  int nthreads) {
+                  int nthreads, int is_fp16) {
   if (B < 0 || H <= 0 || Hk <= 0 || H % Hk != 0 || D <= 0 || block_size <= 0)
     return ORC_BAD_SHAPE;
   int group = H / Hk;
@@ -194,12 +215,13 @@ int oracle_decode(double* out, double* lse, const uint16_t* q, const uint16_t* k
     for (int64_t idx = 0; idx < n; ++idx) {
       int64_t bh = pairs ? pairs[idx] : idx;
       int b = (int)(bh / H), h = (int)(bh % H);
-      for (int d = 0; d < D; ++d) qv[d] = bf16_bits_to_double(q[((int64_t)b * H + h) * D + d]);
+      for (int d = 0; d < D; ++d)
+        qv[d] = elem_to_double(q[((int64_t)b * H + h) * D + d], is_fp16);
       double row_lse;
       int64_t dst = pairs ? idx : bh; /* compact output when a subset is asked for */
       int rc = attend_row(out + dst * D, &row_lse, qv, k_cache, v_cache,
                           block_tables + (int64_t)b * max_blocks, max_blocks, context_lens[b],
-                          Hk, h / group, D, block_size, num_blocks, scale, scores);
+                          Hk, h / group, D, block_size, num_blocks, scale, scores, is_fp16);
       if (lse) lse[dst] = row_lse;
       if (rc != ORC_OK) {
 #pragma omp critical
@@ -222,7 +244,7 @@ int oracle_prefill(double* out, double* lse, const uint16_t* q, const uint16_t* 
                    const uint16_t* v_cache, const int32_t* block_tables, int max_blocks,
                    const int32_t* cu_q, const int32_t* cu_k, int S, int H, int Hk, int D,
                    int block_size, int64_t num_blocks, int causal, double scale,
-                   const int64_t* rows, int64_t num_rows, int nthreads) {
+                   const int64_t* rows, int64_t num_rows, int nthreads, int is_fp16) {
   if (S < 0 || H <= 0 || Hk <= 0 || H % Hk != 0 || D <= 0 || block_size <= 0)
     return ORC_BAD_SHAPE;
   int group = H / Hk;
@@ -260,12 +282,12 @@ int oracle_prefill(double* out, double* lse, const uint16_t* q, const uint16_t* 
       int64_t c_s = k_s - n_s;
       int64_t i = tok - cu_q[s];
       int64_t num_keys = causal ? (c_s + i + 1) : k_s;
-      for (int d = 0; d < D; ++d) qv[d] = bf16_bits_to_double(q[(tok * H + h) * D + d]);
+      for (int d = 0; d < D; ++d) qv[d] = elem_to_double(q[(tok * H + h) * D + d], is_fp16);
       double row_lse;
       int64_t dst = rows ? idx : th; /* compact output when a subset is asked for */
       int rc = attend_row(out + dst * D, &row_lse, qv, k_cache, v_cache,
                           block_tables + (int64_t)s * max_blocks, max_blocks, num_keys, Hk,
-                          h / group, D, block_size, num_blocks, scale, scores);
+                          h / group, D, block_size, num_blocks, scale, scores, is_fp16);
       if (lse) lse[dst] = row_lse;
       if (rc != ORC_OK) {
 #pragma omp critical

@@ -87,23 +87,26 @@ class PagedCase:
         return np.unique(np.concatenate(ids).astype(np.int64))
 
 
-def _bf16(x: np.ndarray) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+def _bf16(x: np.ndarray, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """fp32 values rounded (nearest even) to the 16-bit element type (bf16 or fp16)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dtype)
 
 
 def _fill_blocks(cache: torch.Tensor, ids: np.ndarray, rng: np.random.Generator,
                  chunk: int = 256) -> None:
-    """Fill whole physical blocks `ids` (in that order) with N(0,1) bf16 values."""
+    """Fill whole physical blocks `ids` (in that order) with N(0,1) values of the cache's
+    element type."""
     _, bs, hk, d = cache.shape
     for s in range(0, len(ids), chunk):
         part = ids[s:s + chunk]
         vals = rng.standard_normal((len(part), bs, hk, d), dtype=np.float32)
-        cache[torch.from_numpy(part.astype(np.int64))] = _bf16(vals)
+        cache[torch.from_numpy(part.astype(np.int64))] = _bf16(vals, cache.dtype)
 
 
-def _empty_cache(nb: int, bs: int, hk: int, d: int, poison: bool) -> torch.Tensor:
+def _empty_cache(nb: int, bs: int, hk: int, d: int, poison: bool,
+                 dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
     fill = float("nan") if poison else 0.0
-    return torch.full((nb, bs, hk, d), fill, dtype=torch.bfloat16)
+    return torch.full((nb, bs, hk, d), fill, dtype=dtype)
 
 
 def _poison_tails(cache: torch.Tensor, tables: np.ndarray, lens: np.ndarray, bs: int,
@@ -158,7 +161,8 @@ def decode_case(context_lens: Sequence[int], num_heads: int = 16, num_kv_heads: 
                 head_dim: int = 128, block_size: int = 256, num_blocks: Optional[int] = None,
                 seed: int = SEED_BASE, poison: bool = True, skip_slots: Sequence[int] = (),
                 max_blocks: Optional[int] = None, share_group: int = 0,
-                share_blocks: int = 0, name: str = "decode") -> PagedCase:
+                share_blocks: int = 0, name: str = "decode",
+                dtype: torch.dtype = torch.bfloat16) -> PagedCase:
     """A decode step: each sequence b stores one new token at position len_b - 1 and then
     attends over positions 0..len_b-1. Sequences with len_b == 0 are CUDA-graph padding
     rows: slot -1 and no blocks. Sequences listed in skip_slots get slot -1 too (their
@@ -170,17 +174,17 @@ def decode_case(context_lens: Sequence[int], num_heads: int = 16, num_kv_heads: 
     need = sum(-(-int(n) // bs) for n in lens)
     nb = num_blocks if num_blocks is not None else max(need + 4, 8)
     tables, nshared = _assign_blocks(lens, bs, nb, rng, max_blocks, share_group, share_blocks)
-    k_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison)
-    v_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison)
+    k_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison, dtype)
+    v_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison, dtype)
     used = np.unique(tables[tables >= 0]).astype(np.int64) if B else np.zeros(0, np.int64)
     _fill_blocks(k_cache, used, rng)
     _fill_blocks(v_cache, used, rng)
     if poison:
         _poison_tails(k_cache, tables, lens, bs, float("nan"))
         _poison_tails(v_cache, tables, lens, bs, float("nan"))
-    q = _bf16(rng.standard_normal((B, num_heads, head_dim), dtype=np.float32))
-    k_new = _bf16(rng.standard_normal((B, num_kv_heads, head_dim), dtype=np.float32))
-    v_new = _bf16(rng.standard_normal((B, num_kv_heads, head_dim), dtype=np.float32))
+    q = _bf16(rng.standard_normal((B, num_heads, head_dim), dtype=np.float32), dtype)
+    k_new = _bf16(rng.standard_normal((B, num_kv_heads, head_dim), dtype=np.float32), dtype)
+    v_new = _bf16(rng.standard_normal((B, num_kv_heads, head_dim), dtype=np.float32), dtype)
     slots = np.full(B, -1, np.int32)
     skip = set(int(s) for s in skip_slots)
     for b in range(B):
@@ -198,7 +202,8 @@ def decode_case(context_lens: Sequence[int], num_heads: int = 16, num_kv_heads: 
 def prefill_case(cached: Sequence[int], new: Sequence[int], num_heads: int = 16,
                  num_kv_heads: int = 8, head_dim: int = 128, block_size: int = 256,
                  num_blocks: Optional[int] = None, seed: int = SEED_BASE, poison: bool = True,
-                 causal: bool = True, name: str = "prefill") -> PagedCase:
+                 causal: bool = True, name: str = "prefill",
+                 dtype: torch.dtype = torch.bfloat16) -> PagedCase:
     """A chunked-prefill step: sequence s has cached[s] tokens already in the cache (a
     prefix hit or an earlier chunk) and new[s] new tokens that are stored and then attend
     causally over positions 0..cached[s]+i."""
@@ -211,8 +216,8 @@ def prefill_case(cached: Sequence[int], new: Sequence[int], num_heads: int = 16,
     need = sum(-(-int(t) // bs) for t in total)
     nb = num_blocks if num_blocks is not None else max(need + 4, 8)
     tables, _ = _assign_blocks(total, bs, nb, rng)
-    k_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison)
-    v_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison)
+    k_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison, dtype)
+    v_cache = _empty_cache(nb, bs, num_kv_heads, head_dim, poison, dtype)
     used = np.unique(tables[tables >= 0]).astype(np.int64) if S else np.zeros(0, np.int64)
     _fill_blocks(k_cache, used, rng)
     _fill_blocks(v_cache, used, rng)
@@ -225,9 +230,9 @@ def prefill_case(cached: Sequence[int], new: Sequence[int], num_heads: int = 16,
         _poison_tails(k_cache, tables, total, bs, float("nan"))
         _poison_tails(v_cache, tables, total, bs, float("nan"))
     nq = int(n.sum())
-    q = _bf16(rng.standard_normal((nq, num_heads, head_dim), dtype=np.float32))
-    k_new = _bf16(rng.standard_normal((nq, num_kv_heads, head_dim), dtype=np.float32))
-    v_new = _bf16(rng.standard_normal((nq, num_kv_heads, head_dim), dtype=np.float32))
+    q = _bf16(rng.standard_normal((nq, num_heads, head_dim), dtype=np.float32), dtype)
+    k_new = _bf16(rng.standard_normal((nq, num_kv_heads, head_dim), dtype=np.float32), dtype)
+    v_new = _bf16(rng.standard_normal((nq, num_kv_heads, head_dim), dtype=np.float32), dtype)
     slots = np.empty(nq, np.int32)
     cu_q = np.zeros(S + 1, np.int32)
     cu_k = np.zeros(S + 1, np.int32)

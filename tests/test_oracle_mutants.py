@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_fp16_cpu as f16
 from tests import test_sampler_oracle_cpu as gs
 from tests import test_staged_write_cpu as sw
 
@@ -19,8 +20,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 # (name, text in oracle.c, replacement, pins expected to notice)
 MUTANTS = [
-    ("gqa_modulo", "Hk, h / group, D, block_size, num_blocks, scale, scores);\n      if (lse) lse[dst]",
-     "Hk, h % Hk, D, block_size, num_blocks, scale, scores);\n      if (lse) lse[dst]",
+    ("gqa_modulo", "Hk, h / group, D, block_size, num_blocks, scale, scores, is_fp16);\n      if (lse) lse[dst]",
+     "Hk, h % Hk, D, block_size, num_blocks, scale, scores, is_fp16);\n      if (lse) lse[dst]",
      [pins.test_decode_gqa_head_mapping_with_constant_values]),
     ("no_scale", "scores[t] = scale * dot;", "scores[t] = dot;",
      [pins.test_decode_two_keys_closed_form_scale]),
@@ -59,6 +60,12 @@ MUTANTS = [
      [gs.test_philox_known_answer_vectors]),
     ("uniform_wrong_shift", "(2u * (bits >> 9) + 1u)", "(2u * (bits >> 8) + 1u)",
      [gs.test_uniform_mapping_closed_form]),
+    ("f16_exponent_bias", "else v = ldexp((double)(1024 + m), e - 25);",
+     "else v = ldexp((double)(1024 + m), e - 24);",
+     [f16.test_f16_widening_matches_numpy_on_every_bit_pattern]),
+    ("f16_as_bf16", "return is_fp16 ? f16_bits_to_double(bits) : bf16_bits_to_double(bits);",
+     "return bf16_bits_to_double(bits);",
+     [f16.test_fp16_and_bf16_agree_on_values_exact_in_both]),
     ("ties_to_highest_index", "      if (x > m1) {", "      if (x >= m1) {",
      [gs.test_greedy_is_numpy_argmax_with_lowest_index_on_ties]),
 ]
@@ -73,6 +80,10 @@ def _call(fn):
         return fn(True)
     if "bs" in params:
         return fn(4)
+    if "D" in params and "bs" in params:
+        return fn(64, 16)
+    if "D" in params:
+        return fn(64)
     if "T" in params:
         return fn(0.7)
     if "dtype" in params:
