@@ -337,14 +337,15 @@ def prefill_flops(case) -> float:
     return 4.0 * case.num_heads * case.head_dim * pairs
 
 
-def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None):
+def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128, dtype=None):
     """Chunked-prefill step of workload 5: store of every new token, then causal prefill.
     Returns timings (CUDA events on the stream), TFLOP/s and the fraction of the measured
-    sustained bf16 tensor peak."""
+    sustained bf16 tensor peak (fp16 has the same dense tensor rate)."""
     import torch
     import paged_kv_cache_107_gb300 as pk
     from paged_kv_cache_107_gb300 import workloads
-    case = workloads.workload(5, poison=True, num_blocks=pool_blocks)
+    case = workloads.workload(5, poison=True, num_blocks=pool_blocks, head_dim=head_dim,
+                              dtype=dtype or torch.bfloat16)
     kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
     q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
     slots = torch.from_numpy(case.slot_mapping).to(dev)
@@ -389,6 +390,57 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None):
             "peak_tflops": tflops_peak, "peak_source": f"{src} bf16 dense (sustained)",
             "tokens_per_s": nq / (pf_ms * 1e-3),
             "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
+
+
+def measure_variants(dev, steps: int, warmup: int):
+    """head_dim 64 / IEEE fp16 variants on the shapes of the decode step (workload 2: the
+    fused store + decode, one launch) and of the chunked prefill (workload 5)."""
+    import torch
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300 import workloads
+    hbm_peak, _, peak_src = measured_peaks()
+    res = {"peak_gbs": hbm_peak, "peak_source": f"{peak_src} HBM copy GB/s"}
+    for D, dt, tag in ((64, torch.bfloat16, "d64_bf16"), (64, torch.float16, "d64_fp16"),
+                       (128, torch.float16, "d128_fp16")):
+        case = workloads.workload(2, poison=True, head_dim=D, dtype=dt)
+        tot_ctx, kv_bytes, small_bytes, store_bytes = workload_summary(case)
+        kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+        q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+        slots = torch.from_numpy(case.slot_mapping).to(dev)
+        bt = torch.from_numpy(case.block_tables).to(dev)
+        ctx = torch.from_numpy(case.context_lens).to(dev)
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = pk.DecodeWorkspace(case.num_seqs, case.num_heads, case.num_kv_heads, D, device=dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def step():
+            pk.pa_decode_step(out, q, kn, vn, kc, vc, slots, bt, ctx, workspace=ws, dev_err=err,
+                              stream=stream)
+
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item())} in the {tag} step")
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        alg = kv_bytes + small_bytes + case.slot_mapping.nbytes + store_bytes // 2
+        res["decode_step_" + tag] = {
+            "workload": case.name, "step_us": ms * 1e3,
+            "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+            "achieved_gbs": alg / (ms * 1e-3) / 1e9,
+            "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak}
+        del kc, vc, case
+        res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
+                                                head_dim=D, dtype=dt)
+    return res
 
 
 def measure_sampler(dev, steps: int, warmup: int):
@@ -697,6 +749,7 @@ def run_ours(args):
         line["prefill"] = measure_prefill(dev, steps=min(args.steps, 20), warmup=args.warmup)
         line["staged_write"] = measure_staged(dev, steps=min(args.steps, 50), warmup=args.warmup)
         line["sampler"] = measure_sampler(dev, steps=min(args.steps, 50), warmup=args.warmup)
+        line["variants"] = measure_variants(dev, steps=min(args.steps, 30), warmup=args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(case, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb["gbs"], "unit": "GB/s", "cores": cb["cores"],
@@ -723,6 +776,8 @@ def main():
                     help="skip the secondary chunked-prefill measurement")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill step (for profiler captures)")
+    ap.add_argument("--variants-only", action="store_true",
+                    help="time only the head_dim 64 / fp16 variants")
     ap.add_argument("--sampler-only", action="store_true",
                     help="time only the Gumbel-max sampler (for profiler captures)")
     ap.add_argument("--pool-blocks", type=int, default=None,
@@ -730,6 +785,13 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.variants_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_variants(dev, args.steps, args.warmup)))
     elif args.sampler_only:
         import torch
         import paged_kv_cache_107_gb300 as pk

@@ -21,8 +21,9 @@
  *     current device. The library allocates nothing and frees nothing.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL =
  *     the legacy default stream) and never synchronises the host.
- *   - Element type: bf16 (raw 16-bit storage) for q, k, v, caches and outputs.
- *     head_dim must be 128; anything else returns PA_ERR_UNSUPPORTED.
+ *   - Element type: 16-bit floats (raw 16-bit storage) for q, k, v, caches and outputs:
+ *     bf16, or IEEE binary16 (fp16) where a call takes a `dtype` (pa_dtype). head_dim is
+ *     64 or 128; anything else returns PA_ERR_UNSUPPORTED.
  *   - Layouts are C-contiguous unless a stride argument says otherwise:
  *       k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim]
  *       block_tables      [num_seqs, max_blocks_per_seq] int32, right-padded with -1
@@ -67,8 +68,9 @@ enum pa_dev_error {
   PA_DEV_ERR_STAGED = 32   /* a staged run outside the tensor, or run offsets that decrease */
 };
 
-/* Element types of inputs that are not always bf16 (the sampler's logits). */
-enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 };
+/* Element types: the sampler's logits (F32 or BF16) and the attention calls' q, caches
+ * and outputs (BF16 or F16). */
+enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1, PA_DTYPE_F16 = 2 };
 
 /* Human-readable name of a pa_status value. Never NULL. */
 const char* pa_status_str(int status);
@@ -92,8 +94,8 @@ int pa_version(void);
  *   slot_mapping    device, int32 [num_tokens]; -1 = skip this token.
  *   num_tokens      >= 0 (0 launches nothing and returns PA_OK).
  *
- * The copy is bit-exact. Two tokens with the same slot race (the pages never produce
- * that). A 16-byte vector path is used when k, v, both caches and both strides are
+ * The copy is bit-exact for any 16-bit element type (bf16 or fp16). head_dim 64 or 128.
+ * Two tokens with the same slot race (the pages never produce that). A 16-byte vector path is used when k, v, both caches and both strides are
  * 16-byte aligned; otherwise a 2-byte path gives the same bytes.
  */
 int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t v_tok_stride,
@@ -223,8 +225,12 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  * softmax_scale = 1/sqrt(head_dim)); "3.6 ModelRunner…", section 2 (context_lens =
  * len(seq), i.e. the just-stored token is part of the context).
  *
- *   out             device, bf16 [num_seqs, num_heads, head_dim]; written for every row.
- *   q               device, bf16 [num_seqs, num_heads, head_dim].
+ *   out             device, [num_seqs, num_heads, head_dim]; written for every row.
+ *   q               device, [num_seqs, num_heads, head_dim].
+ *   head_dim        64 or 128.
+ *   dtype           element type of q, both caches and out: PA_DTYPE_BF16 or PA_DTYPE_F16
+ *                   (nano-vllm overview page, section "PagedAttention：KV Cache": a
+ *                   block's cache tensor takes head_dim and dtype as parameters).
  *   block_tables    device, int32 [num_seqs, max_blocks_per_seq]; entries at index
  *                   >= ceil(context_lens[b]/block_size) are never read.
  *   context_lens    device, int32 [num_seqs]; 0 writes a zero row and reads nothing.
@@ -241,13 +247,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *                   with num_seqs <= B and the same num_heads / num_kv_heads. Calls that
  *                   overlap in time must use different workspaces.
  *
- * Arithmetic: bf16 inputs, fp32 products, fp32 online softmax and accumulation, one
- * bf16 round-to-nearest-even at the end.
+ * Arithmetic: 16-bit inputs widened exactly, fp32 products, fp32 online softmax and
+ * accumulation, one round-to-nearest-even to the element type at the end.
  */
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-              int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int dtype,
+              int block_size, int64_t num_blocks, float scale, int grid_ctas, void* workspace,
               size_t workspace_bytes, int* dev_err, void* stream);
 
 /*
@@ -277,7 +283,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  *                   not the slot of that position (or a token of a sequence with context
  *                   length 0) sets PA_DEV_ERR_SLOT and that token is NOT stored (another
  *                   sequence of the same launch might be reading that row).
- *   everything else as pa_decode (same workspace rules; one workspace per call in flight).
+ *   everything else as pa_decode (head_dim, dtype, the workspace rules; one workspace per
+ *   call in flight).
  *
  * The store and the attention share one read of each new row: the CTA that owns a
  * sequence's last key tile copies that row from k_new/v_new into its tile and writes it to
@@ -289,7 +296,7 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
                    int64_t k_new_stride, int64_t v_new_stride, void* k_cache, void* v_cache,
                    const int32_t* slot_mapping, const int32_t* block_tables,
                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
-                   int num_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_heads, int num_kv_heads, int head_dim, int dtype, int block_size,
                    int64_t num_blocks, float scale, int grid_ctas, void* workspace,
                    size_t workspace_bytes, int* dev_err, void* stream);
 
@@ -301,7 +308,8 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
  * running where no device allocator is available or allowed (a plugin inside a host
  * program that owns all device memory, a runtime that forbids allocation after start-up,
  * a caller with a fixed memory budget). This entry point computes exactly what pa_decode
- * computes with the same arguments, minus workspace/workspace_bytes, and allocates
+ * computes with the same arguments and dtype PA_DTYPE_BF16, minus workspace/
+ * workspace_bytes, and allocates
  * nothing: its scratch is one fixed array of 16 MiB in the library's device memory, held
  * by every GPU that loads the library until the process exits.
  *
@@ -333,8 +341,9 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
  * section 2 (new token i of sequence s sits at absolute position
  * num_cached_tokens + i; cu_seqlens_k counts cached plus new tokens).
  *
- *   out             device, bf16 [cu_seqlens_q[num_seqs], num_heads, head_dim].
- *   q               device, bf16, same shape as out.
+ *   out             device, [cu_seqlens_q[num_seqs], num_heads, head_dim].
+ *   q               device, same shape and element type as out.
+ *   head_dim, dtype 64 or 128; PA_DTYPE_BF16 or PA_DTYPE_F16 (q, both caches and out).
  *   k_cache,v_cache device, bf16 caches that ALREADY hold every key/value row of the
  *                   call, the new tokens included (run pa_store_kvcache first).
  *   block_tables    device, int32 [num_seqs, max_blocks_per_seq].
@@ -349,16 +358,16 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
  *   scale           softmax scale; <= 0 or NaN means 1/sqrt(head_dim).
  *
  * Requirements: block_size a multiple of 128, or a divisor of 128 that is a multiple of
- * 8; q, out and both caches 16-byte aligned. Arithmetic: bf16 tensor-core products
- * with fp32 accumulation, fp32 softmax, P rounded to bf16 for the second product, one
- * bf16 rounding of the output.
+ * 8; q, out and both caches 16-byte aligned. Arithmetic: 16-bit tensor-core products
+ * (kind::f16, both operands of one type) with fp32 accumulation, fp32 softmax, P rounded
+ * to the element type for the second product, one rounding of the output.
  */
 int pa_prefill_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, int max_blocks_per_seq,
                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
                       int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
-                      int head_dim, int block_size, int64_t num_blocks, int causal, float scale,
-                      int* dev_err, void* stream);
+                      int head_dim, int dtype, int block_size, int64_t num_blocks, int causal,
+                      float scale, int* dev_err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -66,11 +66,11 @@ def load_library(path: Optional[str] = None):
         lib.pa_store_kvcache.restype = i32
         lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.pa_decode_workspace_size.restype = sz
-        lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64, f32,
-                                  i32, vp, sz, vp, vp]
+        lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i64,
+                                  f32, i32, vp, sz, vp, vp]
         lib.pa_decode.restype = i32
         lib.pa_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, i32, vp, i32,
-                                       i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp]
+                                       i32, i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp]
         lib.pa_decode_step.restype = i32
         lib.pa_sample_workspace_size.argtypes = [i32]
         lib.pa_sample_workspace_size.restype = sz
@@ -80,7 +80,7 @@ def load_library(path: Optional[str] = None):
                                               vp, vp]
         lib.pa_staged_write_apply.restype = i32
         lib.pa_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
-                                          i32, i32, i64, i32, f32, vp, vp]
+                                          i32, i32, i32, i64, i32, f32, vp, vp]
         lib.pa_prefill_varlen.restype = i32
         _lib = lib
         return lib
@@ -121,11 +121,12 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: Optional[int] = 
 def pa_store_kvcache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
                      v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                      dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """k, v [N, Hk, D] bf16 (token stride may exceed Hk*D); caches [nb, bs, Hk, D]."""
-    _need(k, "k", torch.bfloat16, 3)
-    _need(v, "v", torch.bfloat16, 3)
-    _need(k_cache, "k_cache", torch.bfloat16, 4)
-    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    """k, v [N, Hk, D] bf16 or fp16 (token stride may exceed Hk*D); caches [nb, bs, Hk, D]
+    of the same type (the store is a bit copy)."""
+    _need16(k_cache, "k_cache", 4)
+    _need16(v_cache, "v_cache", 4, k_cache.dtype)
+    _need16(k, "k", 3, k_cache.dtype)
+    _need16(v, "v", 3, k_cache.dtype)
     _need(slot_mapping, "slot_mapping", torch.int32, 1)
     nb, bs, hk, d = k_cache.shape
     if not (k_cache.is_contiguous() and v_cache.is_contiguous() and v_cache.shape == k_cache.shape):
@@ -231,7 +232,18 @@ def pa_staged_upload_apply(base: torch.Tensor, packed_host: torch.Tensor,
     _check(rc, "pa_staged_upload_apply")
 
 
-PA_DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+PA_DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+_ATTN_TYPES = (torch.bfloat16, torch.float16)
+
+
+def _need16(t: torch.Tensor, name: str, ndim: int, dtype: Optional[torch.dtype] = None):
+    """A CUDA tensor of 16-bit floats (bf16 or fp16; `dtype` when given)."""
+    if not t.is_cuda:
+        raise PagedAttentionError(f"{name} must be a CUDA tensor")
+    if t.dtype not in _ATTN_TYPES or (dtype is not None and t.dtype != dtype):
+        raise PagedAttentionError(f"{name} must be {dtype or 'bf16 or fp16'}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise PagedAttentionError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
 
 
 def pa_sample_workspace_size(num_seqs: int) -> int:
@@ -324,16 +336,19 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
               scale: Optional[float] = None, grid_ctas: int = 0,
               workspace: Optional[DecodeWorkspace] = None,
               dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """out, q [B, H, D] bf16; caches [nb, bs, Hk, D]; block_tables [B, maxb] int32 (-1
-    padded); context_lens [B] int32."""
-    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
-                            ("k_cache", k_cache, torch.bfloat16, 4),
-                            ("v_cache", v_cache, torch.bfloat16, 4),
+    """out, q [B, H, D] bf16 or fp16 (D = 64 or 128); caches [nb, bs, Hk, D] of the same
+    type; block_tables [B, maxb] int32 (-1 padded); context_lens [B] int32."""
+    _need16(q, "q", 3)
+    for name, t, dt, nd in (("out", out, q.dtype, 3),
+                            ("k_cache", k_cache, q.dtype, 4),
+                            ("v_cache", v_cache, q.dtype, 4),
                             ("block_tables", block_tables, torch.int32, 2),
                             ("context_lens", context_lens, torch.int32, 1)):
         _need(t, name, dt, nd)
         if not t.is_contiguous():
             raise PagedAttentionError(f"{name} must be contiguous")
+    if not q.is_contiguous():
+        raise PagedAttentionError("q must be contiguous")
     B, H, D = q.shape
     nb, bs, hk, d2 = k_cache.shape
     if out.shape != q.shape or d2 != D or v_cache.shape != k_cache.shape:
@@ -344,7 +359,7 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
         workspace = _default_workspace(B, H, hk, D, q.device)
     rc = load_library().pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-        block_tables.shape[1], _ptr(context_lens), B, H, hk, D, bs, nb,
+        block_tables.shape[1], _ptr(context_lens), B, H, hk, D, PA_DTYPE[q.dtype], bs, nb,
         float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(workspace.buffer),
         workspace.nbytes, _ptr(dev_err), _stream(stream))
     _check(rc, "pa_decode")
@@ -361,17 +376,18 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
     pa_store_kvcache(k_new, v_new, ..., slot_mapping) then pa_decode(...). k_new, v_new
     [B, Hk, D] bf16 (token stride a multiple of 8 elements); slot_mapping [B] int32, -1 or
     the slot of position context_lens[b]-1 of sequence b."""
-    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
-                            ("k_cache", k_cache, torch.bfloat16, 4),
-                            ("v_cache", v_cache, torch.bfloat16, 4),
+    _need16(q, "q", 3)
+    for name, t, dt, nd in (("out", out, q.dtype, 3), ("q", q, q.dtype, 3),
+                            ("k_cache", k_cache, q.dtype, 4),
+                            ("v_cache", v_cache, q.dtype, 4),
                             ("block_tables", block_tables, torch.int32, 2),
                             ("context_lens", context_lens, torch.int32, 1),
                             ("slot_mapping", slot_mapping, torch.int32, 1)):
         _need(t, name, dt, nd)
         if not t.is_contiguous():
             raise PagedAttentionError(f"{name} must be contiguous")
-    _need(k_new, "k_new", torch.bfloat16, 3)
-    _need(v_new, "v_new", torch.bfloat16, 3)
+    _need16(k_new, "k_new", 3, q.dtype)
+    _need16(v_new, "v_new", 3, q.dtype)
     B, H, D = q.shape
     nb, bs, hk, d2 = k_cache.shape
     if out.shape != q.shape or d2 != D or v_cache.shape != k_cache.shape:
@@ -386,7 +402,7 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
     rc = load_library().pa_decode_step(
         _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0), v_new.stride(0),
         _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(block_tables),
-        block_tables.shape[1], _ptr(context_lens), B, H, hk, D, bs, nb,
+        block_tables.shape[1], _ptr(context_lens), B, H, hk, D, PA_DTYPE[q.dtype], bs, nb,
         float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(workspace.buffer),
         workspace.nbytes, _ptr(dev_err), _stream(stream))
     _check(rc, "pa_decode_step")
@@ -398,10 +414,12 @@ def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                       cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
                       max_seqlen_k: int, causal: bool = True, scale: Optional[float] = None,
                       dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """out, q [sum n, H, D] bf16; caches hold every key/value row already (store first)."""
-    for name, t, dt, nd in (("out", out, torch.bfloat16, 3), ("q", q, torch.bfloat16, 3),
-                            ("k_cache", k_cache, torch.bfloat16, 4),
-                            ("v_cache", v_cache, torch.bfloat16, 4),
+    """out, q [sum n, H, D] bf16 or fp16 (D = 64 or 128); caches of the same type hold every
+    key/value row already (store first)."""
+    _need16(q, "q", 3)
+    for name, t, dt, nd in (("out", out, q.dtype, 3), ("q", q, q.dtype, 3),
+                            ("k_cache", k_cache, q.dtype, 4),
+                            ("v_cache", v_cache, q.dtype, 4),
                             ("block_tables", block_tables, torch.int32, 2),
                             ("cu_seqlens_q", cu_seqlens_q, torch.int32, 1),
                             ("cu_seqlens_k", cu_seqlens_k, torch.int32, 1)):
@@ -418,7 +436,7 @@ def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     rc = load_library().pa_prefill_varlen(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S, int(max_seqlen_q),
-        int(max_seqlen_k), H, hk, D, bs, nb, 1 if causal else 0,
+        int(max_seqlen_k), H, hk, D, PA_DTYPE[q.dtype], bs, nb, 1 if causal else 0,
         float(scale) if scale is not None else 0.0, _ptr(dev_err), _stream(stream))
     _check(rc, "pa_prefill_varlen")
     return out

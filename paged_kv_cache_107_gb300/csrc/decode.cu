@@ -1,5 +1,6 @@
 // decode.cu — host side of pa_decode: workspace layout, head-slab choice and the
-// launch of the decode kernel (decode_kernel.cuh) without the fused store.
+// launch of the decode kernel (decode_kernel.cuh) without the fused store; head_dim 128
+// with bf16 is instantiated here, the other combinations in decode_d*_*.cu.
 #include "decode_kernel.cuh"
 
 namespace pa {
@@ -36,12 +37,11 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
 }
 
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
-  switch (decode_head_slab(a.num_kv_heads)) {
-    case 8: return dispatch_group<8, false>(a, info, stream);
-    case 4: return dispatch_group<4, false>(a, info, stream);
-    case 2: return dispatch_group<2, false>(a, info, stream);
-    default: return dispatch_group<1, false>(a, info, stream);
-  }
+  if (a.head_dim == 128 && !a.f16) return dispatch_slab<false, 128, false>(a, info, stream);
+  if (a.head_dim == 64) return a.f16 ? launch_decode_d64_f16(a, info, stream)
+                                     : launch_decode_d64_bf16(a, info, stream);
+  if (a.head_dim == 128) return launch_decode_d128_f16(a, info, stream);
+  return PA_ERR_UNSUPPORTED;
 }
 
 }  // namespace pa

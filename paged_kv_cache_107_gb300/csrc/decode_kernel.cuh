@@ -54,18 +54,19 @@ constexpr int kTokPerWarp = 16;
 constexpr int kPairs = kTokPerWarp / 2;  // token pairs (one per half-warp) per warp and tile
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagWhole = 4;
 
-template <int HS, int G>
+template <int HS, int G, int D>
 struct DecCfg {
+  static constexpr int DPL = D / 16;                // dims per lane (a half-warp per row)
   static constexpr int T = 128 / HS;                // tokens per stage
   static constexpr int WPH = kConsumerWarps / HS;   // consumer warps per KV head
-  static constexpr int ROW = HS * kHeadDim * 2;     // bytes of one token row of the slab
+  static constexpr int ROW = HS * D * 2;            // bytes of one token row of the slab
   static constexpr int KV_BYTES = T * ROW;          // K (or V) bytes per stage
-  static constexpr int Q_BYTES = HS * G * kHeadDim * 2;
+  static constexpr int Q_BYTES = HS * G * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
   static constexpr int STAGES = (3 * STAGE_BYTES + 8192 <= 227 * 1024) ? 3 : 2;
   static constexpr int NV = kPairs * G;             // partial scores per lane per tile
   static constexpr int CF = NV >= 16 ? NV / 16 : 1;  // scores per lane after the reduction
-  static constexpr int MERGE_FLOATS = G * (kHeadDim + 2);
+  static constexpr int MERGE_FLOATS = G * (D + 2);
   static constexpr int PBUF_FLOATS = 2 * kPairs * G;  // per warp: [half][pair][head]
   static constexpr int CTRL_BYTES = 4096 + kConsumerWarps * PBUF_FLOATS * 4;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + CTRL_BYTES + 128;
@@ -178,15 +179,67 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
       : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
   return *reinterpret_cast<const float2*>(&d);
 }
-// Two bf16 (element 0 in the low half) widened to an fp32 pair.
-__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+// Two 16-bit elements (element 0 in the low half) widened to an fp32 pair: bf16 is the
+// top half of an fp32 (a shift or a mask), IEEE fp16 converts in hardware.
+template <bool F16>
+__device__ __forceinline__ float2 elt2_f2(uint32_t w) {
+  if constexpr (F16) {
+    float lo, hi;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+    return make_float2(lo, hi);
+  } else {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+}
+// Round-to-nearest-even packing of an fp32 pair into two 16-bit elements.
+template <bool F16>
+__device__ __forceinline__ uint32_t f2_elt2(float lo, float hi) {
+  if constexpr (F16) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  } else {
+    return f32x2_to_bf16x2(lo, hi);
+  }
 }
 
-template <int HS, int G, bool FUSED>
+// DPL consecutive 16-bit elements of one lane (DPL/2 words): 16 or 8 bytes.
+template <int DPL>
+struct LaneVec {
+  uint32_t w[DPL / 2];
+};
+template <int DPL>
+__device__ __forceinline__ LaneVec<DPL> ld_lane(const void* p) {
+  LaneVec<DPL> v;
+  if constexpr (DPL == 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    v.w[0] = u.x, v.w[1] = u.y, v.w[2] = u.z, v.w[3] = u.w;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    v.w[0] = u.x, v.w[1] = u.y;
+  }
+  return v;
+}
+template <int DPL>
+__device__ __forceinline__ void st_lane(void* p, const LaneVec<DPL>& v) {
+  if constexpr (DPL == 8) *reinterpret_cast<uint4*>(p) = make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]);
+  else *reinterpret_cast<uint2*>(p) = make_uint2(v.w[0], v.w[1]);
+}
+template <int DPL>
+__device__ __forceinline__ LaneVec<DPL> zero_lane() {
+  LaneVec<DPL> v;
+#pragma unroll
+  for (int i = 0; i < DPL / 2; ++i) v.w[i] = 0u;
+  return v;
+}
+
+template <int HS, int G, bool FUSED, int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_kernel(const DecodeArgs a) {
-  using C = DecCfg<HS, G>;
+  using C = DecCfg<HS, G, D>;
+  constexpr int DPL = C::DPL;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -260,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
       if (load_ctx(a.context_lens, b, cap) != 0) continue;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                            ((int64_t)b * H + slab * heads_per_slab) * kHeadDim);
-      const int nvec = heads_per_slab * kHeadDim / 8;
+                                            ((int64_t)b * H + slab * heads_per_slab) * D);
+      const int nvec = heads_per_slab * D / 8;
       for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -317,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t policy = policy_evict_first();
     const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
     const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
-    const int64_t row_elems = (int64_t)Hk * kHeadDim;
-    const int64_t slab_off = (int64_t)slab * HS * kHeadDim;
+    const int64_t row_elems = (int64_t)Hk * D;
+    const int64_t slab_off = (int64_t)slab * HS * D;
     int b = ctl.b0;
     int64_t pb = ctl.pb0;
     int ctx_b = load_ctx(a.context_lens, b, cap);
@@ -368,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The rows of a tile are one contiguous run when the slab is every KV head and the
       // tile sits inside one block: then lane 0 moves K and V with one copy each.
       const int pos_first = tok0, pos_last = tok0 + count - 1;
-      const bool one_run = slab_off == 0 && row_elems == (int64_t)HS * kHeadDim &&
+      const bool one_run = slab_off == 0 && row_elems == (int64_t)HS * D &&
                            count > 0 && (pos_first / a.block_size) == (pos_last / a.block_size);
       const uint16_t* src[ROWS_PER_LANE];
       int ok_rows = 0;
@@ -465,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (first && lane == 0) {
         const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) +
-                               ((int64_t)b * H + (int64_t)slab * HS * G) * kHeadDim;
+                               ((int64_t)b * H + (int64_t)slab * HS * G) * D;
         bulk_g2s(st + 2 * C::KV_BYTES, qsrc, C::Q_BYTES, &ctl.full[s]);
       }
     }
@@ -487,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = bfly_base<C::NV>(sub);
   float* pbuf = pbuf_all + warp * C::PBUF_FLOATS;
 
-  float2 qp[G][4];  // q of the group's heads, this lane's 8 dims, pre-scaled
-  float2 op[G][4];  // running output, this lane's 8 dims
+  float2 qp[G][DPL / 2];  // q of the group's heads, this lane's DPL dims, pre-scaled
+  float2 op[G][DPL / 2];  // running output, this lane's DPL dims
   float m_run[G];
   float m_own[C::CF];
   float l_loc[C::CF];
@@ -496,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int hh = 0; hh < G; ++hh) {
     m_run[hh] = -INFINITY;
 #pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = make_float2(0.f, 0.f), qp[hh][c2] = op[hh][c2];
+    for (int c2 = 0; c2 < DPL / 2; ++c2) op[hh][c2] = make_float2(0.f, 0.f), qp[hh][c2] = op[hh][c2];
   }
 #pragma unroll
   for (int r = 0; r < C::CF; ++r) m_own[r] = -INFINITY, l_loc[r] = 0.f;
@@ -520,13 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* Qst = Kst + 2 * C::KV_BYTES;
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(Qst + ((j * G + hh) * kHeadDim + sub * 8) * 2);
-        qp[hh][0] = mul2(bf16x2_f2(qv.x), scale2);
-        qp[hh][1] = mul2(bf16x2_f2(qv.y), scale2);
-        qp[hh][2] = mul2(bf16x2_f2(qv.z), scale2);
-        qp[hh][3] = mul2(bf16x2_f2(qv.w), scale2);
+        const LaneVec<DPL> qv = ld_lane<DPL>(Qst + ((j * G + hh) * D + sub * DPL) * 2);
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = make_float2(0.f, 0.f);
+        for (int c2 = 0; c2 < DPL / 2; ++c2) qp[hh][c2] = mul2(elt2_f2<F16>(qv.w[c2]), scale2);
+#pragma unroll
+        for (int c2 = 0; c2 < DPL / 2; ++c2) op[hh][c2] = make_float2(0.f, 0.f);
         m_run[hh] = -INFINITY;
       }
 #pragma unroll
@@ -534,41 +585,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- this warp's rows of the tile: K now, V early (in-bounds shared loads) ---------
-    uint4 kraw[kPairs], vraw[kPairs];
+    LaneVec<DPL> kraw[kPairs], vraw[kPairs];
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
       const int t = w * kTokPerWarp + 2 * i + half;
-      const size_t off = (size_t)(t * HS + j) * (kHeadDim * 2) + sub * 16;
-      kraw[i] = *reinterpret_cast<const uint4*>(Kst + off);
-      vraw[i] = *reinterpret_cast<const uint4*>(Vst + off);
-      if (t >= count) vraw[i] = make_uint4(0u, 0u, 0u, 0u);  // stale rows must not reach p*v
+      const size_t off = (size_t)(t * HS + j) * (D * 2) + sub * (DPL * 2);
+      kraw[i] = ld_lane<DPL>(Kst + off);
+      vraw[i] = ld_lane<DPL>(Vst + off);
+      if (t >= count) vraw[i] = zero_lane<DPL>();  // stale rows must not reach p*v
     }
     if constexpr (FUSED) {
       // the new token's row of KV head kvh: its half-warp writes it to the cache slot
       if (meta.new_row >= 0) {
-        const int64_t dst = meta.new_slot * ((int64_t)Hk * kHeadDim) + (int64_t)kvh * kHeadDim + sub * 8;
+        const int64_t dst = meta.new_slot * ((int64_t)Hk * D) + (int64_t)kvh * D + sub * DPL;
 #pragma unroll
         for (int i = 0; i < kPairs; ++i) {
           if (w * kTokPerWarp + 2 * i + half == meta.new_row) {
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(const_cast<void*>(a.k_cache)) + dst) = kraw[i];
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(const_cast<void*>(a.v_cache)) + dst) = vraw[i];
+            st_lane<DPL>(static_cast<uint16_t*>(const_cast<void*>(a.k_cache)) + dst, kraw[i]);
+            st_lane<DPL>(static_cast<uint16_t*>(const_cast<void*>(a.v_cache)) + dst, vraw[i]);
           }
         }
       }
     }
 
-    // ---- scores: q . k, 8 dims per lane, reduced over the 16 lanes of a row ------------
+    // ---- scores: q . k, DPL dims per lane, reduced over the 16 lanes of a row ----------
     float sc[C::NV];
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
-      const float2 k0 = bf16x2_f2(kraw[i].x), k1 = bf16x2_f2(kraw[i].y);
-      const float2 k2 = bf16x2_f2(kraw[i].z), k3 = bf16x2_f2(kraw[i].w);
+      float2 kf[DPL / 2];
+#pragma unroll
+      for (int c2 = 0; c2 < DPL / 2; ++c2) kf[c2] = elt2_f2<F16>(kraw[i].w[c2]);
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        float2 acc = mul2(qp[hh][0], k0);
-        acc = fma2(qp[hh][1], k1, acc);
-        acc = fma2(qp[hh][2], k2, acc);
-        acc = fma2(qp[hh][3], k3, acc);
+        float2 acc = mul2(qp[hh][0], kf[0]);
+#pragma unroll
+        for (int c2 = 1; c2 < DPL / 2; ++c2) acc = fma2(qp[hh][c2], kf[c2], acc);
         sc[i * G + hh] = acc.x + acc.y;
       }
     }
@@ -629,32 +680,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < G; ++hh) {
         const float2 al2 = make_float2(alpha[hh], alpha[hh]);
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) op[hh][c2] = mul2(op[hh][c2], al2);
+        for (int c2 = 0; c2 < DPL / 2; ++c2) op[hh][c2] = mul2(op[hh][c2], al2);
       }
     }
     // ---- o += p v ----------------------------------------------------------------------
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
-      const float2 v0 = bf16x2_f2(vraw[i].x), v1 = bf16x2_f2(vraw[i].y);
-      const float2 v2 = bf16x2_f2(vraw[i].z), v3 = bf16x2_f2(vraw[i].w);
+      float2 vf[DPL / 2];
+#pragma unroll
+      for (int c2 = 0; c2 < DPL / 2; ++c2) vf[c2] = elt2_f2<F16>(vraw[i].w[c2]);
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
         const float2 p2 = make_float2(pv[i * G + hh], pv[i * G + hh]);
-        op[hh][0] = fma2(p2, v0, op[hh][0]);
-        op[hh][1] = fma2(p2, v1, op[hh][1]);
-        op[hh][2] = fma2(p2, v2, op[hh][2]);
-        op[hh][3] = fma2(p2, v3, op[hh][3]);
+#pragma unroll
+        for (int c2 = 0; c2 < DPL / 2; ++c2) op[hh][c2] = fma2(p2, vf[c2], op[hh][c2]);
       }
     }
 
     if (meta.flags & kFlagLast) {
       // ---- finalize the segment ----------------------------------------------------
       // (1) fold the two half-warps (tokens 2i and 2i+1) and total the softmax sums
-      float o[G][8];
+      float o[G][DPL];
 #pragma unroll
       for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) {
+        for (int c2 = 0; c2 < DPL / 2; ++c2) {
           o[hh][2 * c2] = op[hh][c2].x + __shfl_xor_sync(0xffffffffu, op[hh][c2].x, 16);
           o[hh][2 * c2 + 1] = op[hh][c2].y + __shfl_xor_sync(0xffffffffu, op[hh][c2].y, 16);
         }
@@ -691,16 +741,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (half == 0) {
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
-            float4* d4 = reinterpret_cast<float4*>(mine + hh * kHeadDim + sub * 8);
-            d4[0] = make_float4(o[hh][0], o[hh][1], o[hh][2], o[hh][3]);
-            d4[1] = make_float4(o[hh][4], o[hh][5], o[hh][6], o[hh][7]);
+            float4* d4 = reinterpret_cast<float4*>(mine + hh * D + sub * DPL);
+#pragma unroll
+            for (int q4 = 0; q4 < DPL / 4; ++q4)
+              d4[q4] = make_float4(o[hh][4 * q4], o[hh][4 * q4 + 1], o[hh][4 * q4 + 2], o[hh][4 * q4 + 3]);
           }
         }
         if (lane == 0) {
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
-            mine[G * kHeadDim + hh] = m_run[hh];
-            mine[G * kHeadDim + G + hh] = l_all[hh];
+            mine[G * D + hh] = m_run[hh];
+            mine[G * D + G + hh] = l_all[hh];
           }
         }
         fence_proxy_async_smem();
@@ -719,16 +770,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* other = merge + (size_t)(w2 - 1) * C::MERGE_FLOATS;
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
-            const float m2 = other[G * kHeadDim + hh];
-            const float l2 = other[G * kHeadDim + G + hh];
+            const float m2 = other[G * D + hh];
+            const float l2 = other[G * D + G + hh];
             const float mm = fmaxf(m_run[hh], m2);
             const float a1 = (mm == -INFINITY) ? 0.f : fast_exp2(m_run[hh] - mm);
             const float a2 = (mm == -INFINITY) ? 0.f : fast_exp2(m2 - mm);
-            const float4 p0 = lds128f(other + hh * kHeadDim + sub * 8);
-            const float4 p1 = lds128f(other + hh * kHeadDim + sub * 8 + 4);
-            const float ov[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            float ov[DPL];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[hh][e] = o[hh][e] * a1 + ov[e] * a2;
+            for (int q4 = 0; q4 < DPL / 4; ++q4) {
+              const float4 p4 = lds128f(other + hh * D + sub * DPL + 4 * q4);
+              ov[4 * q4] = p4.x, ov[4 * q4 + 1] = p4.y, ov[4 * q4 + 2] = p4.z, ov[4 * q4 + 3] = p4.w;
+            }
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[hh][e] = o[hh][e] * a1 + ov[e] * a2;
             l_all[hh] = l_all[hh] * a1 + l2 * a2;
             m_run[hh] = mm;
           }
@@ -741,13 +795,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int hh = 0; hh < G; ++hh) {
               const int hg = kvh * G + hh;
               const float inv = l_all[hh] > 0.f ? 1.f / l_all[hh] : 0.f;
-              uint4 pk;
-              pk.x = f32x2_to_bf16x2(o[hh][0] * inv, o[hh][1] * inv);
-              pk.y = f32x2_to_bf16x2(o[hh][2] * inv, o[hh][3] * inv);
-              pk.z = f32x2_to_bf16x2(o[hh][4] * inv, o[hh][5] * inv);
-              pk.w = f32x2_to_bf16x2(o[hh][6] * inv, o[hh][7] * inv);
-              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                        ((int64_t)b * H + hg) * kHeadDim + sub * 8) = pk;
+              LaneVec<DPL> pk;
+#pragma unroll
+              for (int c2 = 0; c2 < DPL / 2; ++c2)
+                pk.w[c2] = f2_elt2<F16>(o[hh][2 * c2] * inv, o[hh][2 * c2 + 1] * inv);
+              st_lane<DPL>(static_cast<uint16_t*>(a.out) + ((int64_t)b * H + hg) * D + sub * DPL, pk);
             }
           }
         } else {
@@ -758,9 +810,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int hg = kvh * G + hh;
               const float inv = l_all[hh] > 0.f ? 1.f / l_all[hh] : 0.f;
               float4* d4 = reinterpret_cast<float4*>(
-                  a.part_o + (((int64_t)c * 2 + slot) * H + hg) * kHeadDim + sub * 8);
-              d4[0] = make_float4(o[hh][0] * inv, o[hh][1] * inv, o[hh][2] * inv, o[hh][3] * inv);
-              d4[1] = make_float4(o[hh][4] * inv, o[hh][5] * inv, o[hh][6] * inv, o[hh][7] * inv);
+                  a.part_o + (((int64_t)c * 2 + slot) * H + hg) * D + sub * DPL);
+#pragma unroll
+              for (int q4 = 0; q4 < DPL / 4; ++q4)
+                d4[q4] = make_float4(o[hh][4 * q4] * inv, o[hh][4 * q4 + 1] * inv,
+                                     o[hh][4 * q4 + 2] * inv, o[hh][4 * q4 + 3] * inv);
             }
           }
           if (lane == 0) {
@@ -796,7 +850,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              constexpr int CPL = D / 32;  // combined dims per lane
+              float acc[CPL];
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
               float den = 0.f;
               for (int k0 = 0; k0 < nseg; k0 += 32) {
                 const int64_t c2 = c_lo + k0 + lane;
@@ -814,21 +871,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int64_t ck = c_lo + k0 + k;
                   den += wk;
                   if (wk != 0.f) {
-                    const float4 po = __ldcg(reinterpret_cast<const float4*>(
-                        a.part_o + ((ck * 2 + slk) * H + hg) * kHeadDim) + lane);
-                    acc.x = fmaf(wk, po.x, acc.x);
-                    acc.y = fmaf(wk, po.y, acc.y);
-                    acc.z = fmaf(wk, po.z, acc.z);
-                    acc.w = fmaf(wk, po.w, acc.w);
+                    const float* src = a.part_o + ((ck * 2 + slk) * H + hg) * D + lane * CPL;
+                    if constexpr (CPL == 4) {
+                      const float4 po = __ldcg(reinterpret_cast<const float4*>(src));
+                      acc[0] = fmaf(wk, po.x, acc[0]);
+                      acc[1] = fmaf(wk, po.y, acc[1]);
+                      acc[2] = fmaf(wk, po.z, acc[2]);
+                      acc[3] = fmaf(wk, po.w, acc[3]);
+                    } else {
+                      const float2 po = __ldcg(reinterpret_cast<const float2*>(src));
+                      acc[0] = fmaf(wk, po.x, acc[0]);
+                      acc[1] = fmaf(wk, po.y, acc[1]);
+                    }
                   }
                 }
               }
               const float inv = den > 0.f ? 1.f / den : 0.f;
-              uint2 pk;
-              pk.x = f32x2_to_bf16x2(acc.x * inv, acc.y * inv);
-              pk.y = f32x2_to_bf16x2(acc.z * inv, acc.w * inv);
-              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) +
-                                        ((int64_t)b * H + hg) * kHeadDim + lane * 4) = pk;
+              uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)b * H + hg) * D + lane * CPL;
+              if constexpr (CPL == 4) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(f2_elt2<F16>(acc[0] * inv, acc[1] * inv),
+                                                            f2_elt2<F16>(acc[2] * inv, acc[3] * inv));
+              } else {
+                *reinterpret_cast<uint32_t*>(dst) = f2_elt2<F16>(acc[0] * inv, acc[1] * inv);
+              }
             }
             if (lane == 0) *counter = 0;  // leave the counter zero for the next call
           }
@@ -842,32 +907,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HS, int G, bool FUSED>
+template <int HS, int G, bool FUSED, int D, bool F16>
 int launch_decode_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
-  using C = DecCfg<HS, G>;
+  using C = DecCfg<HS, G, D>;
   static bool attr_done[64] = {false};
   const int dev = info.device;
   if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<HS, G, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(paged_decode_kernel<HS, G, FUSED, D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_done[dev] = true;
   }
   const int slabs = a.num_kv_heads / HS;
   dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);
-  paged_decode_kernel<HS, G, FUSED><<<grid, kThreads, C::SMEM, stream>>>(a);
+  paged_decode_kernel<HS, G, FUSED, D, F16><<<grid, kThreads, C::SMEM, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-template <int HS, bool FUSED>
+template <int HS, bool FUSED, int D, bool F16>
 int dispatch_group(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
   switch (a.num_heads / a.num_kv_heads) {
-    case 1: return launch_decode_t<HS, 1, FUSED>(a, info, stream);
-    case 2: return launch_decode_t<HS, 2, FUSED>(a, info, stream);
-    case 4: return launch_decode_t<HS, 4, FUSED>(a, info, stream);
-    case 8: return launch_decode_t<HS, 8, FUSED>(a, info, stream);
+    case 1: return launch_decode_t<HS, 1, FUSED, D, F16>(a, info, stream);
+    case 2: return launch_decode_t<HS, 2, FUSED, D, F16>(a, info, stream);
+    case 4: return launch_decode_t<HS, 4, FUSED, D, F16>(a, info, stream);
+    case 8: return launch_decode_t<HS, 8, FUSED, D, F16>(a, info, stream);
     default: return PA_ERR_UNSUPPORTED;
+  }
+}
+
+// Every head slab for one (FUSED, D, element type) combination.
+template <bool FUSED, int D, bool F16>
+int dispatch_slab(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
+  switch (decode_head_slab(a.num_kv_heads)) {
+    case 8: return dispatch_group<8, FUSED, D, F16>(a, info, stream);
+    case 4: return dispatch_group<4, FUSED, D, F16>(a, info, stream);
+    case 2: return dispatch_group<2, FUSED, D, F16>(a, info, stream);
+    default: return dispatch_group<1, FUSED, D, F16>(a, info, stream);
   }
 }
 

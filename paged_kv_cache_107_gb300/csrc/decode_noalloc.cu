@@ -57,7 +57,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
       num_blocks <= 0 || max_blocks_per_seq < 0 || grid_ctas < 0)
     return PA_ERR_SHAPE;
   if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
-  if (head_dim != pa::kHeadDimApi || !pa::decode_supported(num_heads, num_kv_heads))
+  if (!pa::head_dim_supported(head_dim) || !pa::decode_supported(num_heads, num_kv_heads))
     return PA_ERR_UNSUPPORTED;
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
@@ -104,5 +104,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   a.part_lse = reinterpret_cast<float*>(ws + off_l);
   a.part_o = reinterpret_cast<float*>(ws + off_o);
   a.dev_err = dev_err;
+  a.head_dim = head_dim;
+  a.f16 = 0;  // bf16
   return pa::launch_decode(a, info, st);
 }

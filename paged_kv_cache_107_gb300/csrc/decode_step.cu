@@ -5,12 +5,11 @@
 namespace pa {
 
 int launch_decode_step(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
-  switch (decode_head_slab(a.num_kv_heads)) {
-    case 8: return dispatch_group<8, true>(a, info, stream);
-    case 4: return dispatch_group<4, true>(a, info, stream);
-    case 2: return dispatch_group<2, true>(a, info, stream);
-    default: return dispatch_group<1, true>(a, info, stream);
-  }
+  if (a.head_dim == 128 && !a.f16) return dispatch_slab<true, 128, false>(a, info, stream);
+  if (a.head_dim == 64) return a.f16 ? launch_decode_step_d64_f16(a, info, stream)
+                                     : launch_decode_step_d64_bf16(a, info, stream);
+  if (a.head_dim == 128) return launch_decode_step_d128_f16(a, info, stream);
+  return PA_ERR_UNSUPPORTED;
 }
 
 }  // namespace pa

@@ -66,7 +66,7 @@ int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t
                      int* dev_err, void* stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0)
     return PA_ERR_SHAPE;
-  if (head_dim != pa::kHeadDimApi) return PA_ERR_UNSUPPORTED;
+  if (!pa::head_dim_supported(head_dim)) return PA_ERR_UNSUPPORTED;
   const int64_t row = (int64_t)num_kv_heads * head_dim;
   if (k_tok_stride < row || v_tok_stride < row) return PA_ERR_SHAPE;
   if (num_tokens == 0) return PA_OK;
@@ -154,7 +154,7 @@ int pa_gumbel_sample(int64_t* out, const void* logits, int64_t row_stride, int l
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim) {
-  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim != pa::kHeadDimApi)
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || !pa::head_dim_supported(head_dim))
     return 0;
   pa::DeviceInfo info;
   if (!pa::current_device_info(&info)) return 0;
@@ -181,14 +181,16 @@ struct StepInput {
 static int decode_entry(void* out, const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_tables, int max_blocks_per_seq,
                         const int32_t* context_lens, int num_seqs, int num_heads,
-                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                        float scale, int grid_ctas, void* workspace, size_t workspace_bytes,
-                        int* dev_err, void* stream, const StepInput* step) {
+                        int num_kv_heads, int head_dim, int dtype, int block_size,
+                        int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+                        size_t workspace_bytes, int* dev_err, void* stream,
+                        const StepInput* step) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || grid_ctas < 0)
     return PA_ERR_SHAPE;
   if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
-  if (head_dim != kHeadDimApi || !decode_supported(num_heads, num_kv_heads))
+  if (!head_dim_supported(head_dim) || !decode_supported(num_heads, num_kv_heads) ||
+      (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16))
     return PA_ERR_UNSUPPORTED;
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (step) {
@@ -232,6 +234,8 @@ static int decode_entry(void* out, const void* q, const void* k_cache, const voi
   a.block_size = block_size;
   a.num_blocks = num_blocks;
   a.scale_log2 = resolve_scale(scale, head_dim);
+  a.head_dim = head_dim;
+  a.f16 = dtype == PA_DTYPE_F16;
   a.grid_ctas = grid_ctas;
   a.counters = reinterpret_cast<int*>(ws + off_c);
   a.part_lse = reinterpret_cast<float*>(ws + off_l);
@@ -254,41 +258,42 @@ extern "C" {
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-              int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int dtype,
+              int block_size, int64_t num_blocks, float scale, int grid_ctas, void* workspace,
               size_t workspace_bytes, int* dev_err, void* stream) {
   return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                          num_blocks, scale, grid_ctas, workspace, workspace_bytes, dev_err,
-                          stream, nullptr);
+                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, dtype,
+                          block_size, num_blocks, scale, grid_ctas, workspace, workspace_bytes,
+                          dev_err, stream, nullptr);
 }
 
 int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
                    int64_t k_new_stride, int64_t v_new_stride, void* k_cache, void* v_cache,
                    const int32_t* slot_mapping, const int32_t* block_tables,
                    int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
-                   int num_heads, int num_kv_heads, int head_dim, int block_size,
+                   int num_heads, int num_kv_heads, int head_dim, int dtype, int block_size,
                    int64_t num_blocks, float scale, int grid_ctas, void* workspace,
                    size_t workspace_bytes, int* dev_err, void* stream) {
   const pa::StepInput step{k_new, v_new, k_new_stride, v_new_stride, slot_mapping};
   return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                          num_blocks, scale, grid_ctas, workspace, workspace_bytes, dev_err,
-                          stream, &step);
+                          context_lens, num_seqs, num_heads, num_kv_heads, head_dim, dtype,
+                          block_size, num_blocks, scale, grid_ctas, workspace, workspace_bytes,
+                          dev_err, stream, &step);
 }
 
 int pa_prefill_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, int max_blocks_per_seq,
                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs,
                       int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
-                      int head_dim, int block_size, int64_t num_blocks, int causal, float scale,
-                      int* dev_err, void* stream) {
+                      int head_dim, int dtype, int block_size, int64_t num_blocks, int causal,
+                      float scale, int* dev_err, void* stream) {
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
     return PA_ERR_SHAPE;
   if (num_heads % num_kv_heads != 0) return PA_ERR_SHAPE;
-  if (head_dim != pa::kHeadDimApi ||
-      !pa::prefill_supported(num_heads, num_kv_heads, block_size))
+  if (!pa::head_dim_supported(head_dim) ||
+      !pa::prefill_supported(num_heads, num_kv_heads, block_size) ||
+      (dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16))
     return PA_ERR_UNSUPPORTED;
   if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (max_seqlen_k > (int64_t)max_blocks_per_seq * block_size) return PA_ERR_SHAPE;
@@ -318,6 +323,8 @@ int pa_prefill_varlen(void* out, const void* q, const void* k_cache, const void*
   a.num_blocks = num_blocks;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = pa::resolve_scale(scale, head_dim);
+  a.head_dim = head_dim;
+  a.f16 = dtype == PA_DTYPE_F16;
   a.dev_err = dev_err;
   return pa::launch_prefill(a, info, static_cast<cudaStream_t>(stream));
 }

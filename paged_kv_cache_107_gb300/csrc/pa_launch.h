@@ -1,6 +1,7 @@
 // pa_launch.h — internal host-side launchers behind the C ABI (not exported).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -9,8 +10,9 @@
 
 namespace pa {
 
-// The only head_dim the kernels are built for.
+// The head dims the kernels are built for.
 constexpr int kHeadDimApi = 128;
+inline bool head_dim_supported(int d) { return d == 64 || d == 128; }
 
 struct DeviceInfo {
   int device;
@@ -60,6 +62,8 @@ struct DecodeArgs {
   int64_t num_blocks;
   float scale_log2;  // softmax scale * log2(e)
   int grid_ctas;     // CTAs along the key stream (per head slab)
+  int head_dim;      // 64 or 128
+  int f16;           // element type of q, caches, out: 0 = bf16, 1 = IEEE fp16
   int* counters;     // [num_seqs * num_kv_heads]
   // fused store (pa_decode_step only; null / 0 otherwise): token b's rows, its slot
   const void* k_new;
@@ -82,6 +86,14 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
 int decode_head_slab(int num_kv_heads);
 bool decode_supported(int num_heads, int num_kv_heads);
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+// The decode (and fused-step) instantiations other than head_dim 128 with bf16, one
+// translation unit each.
+int launch_decode_d64_bf16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+int launch_decode_d64_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+int launch_decode_d128_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+int launch_decode_step_d64_bf16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+int launch_decode_step_d64_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+int launch_decode_step_d128_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
 // The same kernel with the store of token b (k_new/v_new row b) at slot_mapping[b] fused in;
 // the caches are written, so a.k_cache / a.v_cache must point to writable memory.
 int launch_decode_step(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
@@ -104,10 +116,19 @@ struct PrefillArgs {
   int64_t num_blocks;
   int causal;
   float scale_log2;
+  int head_dim;  // 64 or 128
+  int f16;       // element type of q, caches, out: 0 = bf16, 1 = IEEE fp16
   int* dev_err;
 };
 
 bool prefill_supported(int num_heads, int num_kv_heads, int block_size);
 int launch_prefill(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream);
+// The prefill instantiations other than head_dim 128 with bf16, one translation unit each.
+int launch_prefill_d64_bf16(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream,
+                            const CUtensorMap& mk, const CUtensorMap& mv);
+int launch_prefill_d64_f16(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream,
+                           const CUtensorMap& mk, const CUtensorMap& mv);
+int launch_prefill_d128_f16(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream,
+                            const CUtensorMap& mk, const CUtensorMap& mv);
 
 }  // namespace pa

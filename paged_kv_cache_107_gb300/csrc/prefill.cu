@@ -1,424 +1,10 @@
-// prefill.cu — chunked (varlen, causal) prefill attention over the paged cache on the
-// tcgen05 tensor cores.
-//
-// What it computes ("nano-vllm解读", section "如何适配不同请求不同序列长度"; "3.6 ModelRunner、
-// CUDA Graph 与性能基准", section 2): for sequence s with n_s new tokens (rows
-// cu_seqlens_q[s]..) and k_s = cu_seqlens_k[s+1]-cu_seqlens_k[s] keys (c_s = k_s - n_s cached
-// ones first), new token i sits at absolute position c_s + i and attends, per query head
-// h, over keys t <= c_s + i (causal) or all k_s keys, read through block_tables[s]:
-// o = softmax(scale * q K^T) V.
-//
-// GB300 design (one CTA per (KV head j, sequence s, pair of 128-row query tiles)):
-//  * A 128-row query tile is 128/G positions x the G query heads of KV group j (G = H/H_kv),
-//    so every K/V tile fetched for the group serves all of its heads. A CTA holds two such
-//    tiles (A: the earlier positions, B: the next ones) that take turns on the tensor core:
-//    while one softmax warpgroup works, the other tile's products run.
-//  * TMA: K and V are described by 4-D tensor maps over [num_blocks, block_size, H_kv, D];
-//    a box of (64 dims x 1 head x R rows x 1 block), 128-byte swizzled, takes the physical
-//    block id from the block table as a coordinate. A K/V tile is 128 keys (R = 128 when
-//    block_size >= 128, else several blocks). K has a 3-deep ring, V a 2-deep one; K runs
-//    one tile ahead of V.
-//  * tcgen05.mma (kind::f16, bf16 operands, fp32 accumulators in tensor memory, all 512
-//    columns): S_g = Q_g K^T (A = Q and B = K from shared memory, K-major) in 128 columns per
-//    tile; the softmax writes P back over S as packed bf16 and O_g += P V reads P straight
-//    from tensor memory (B = V, MN-major) into 128 more columns per tile. On the tensor core
-//    the order per key tile is PV_A(i), S_A(i+1), PV_B(i), S_B(i+1): each S is issued only
-//    after the PV that reads the P it overwrites, and S_g(i) completes after PV_g(i-1), so
-//    O_g is stable whenever the softmax sees a new S_g. Key tiles past the causal limit of
-//    tile A are not multiplied for A.
-//  * Softmax: 8 warps, thread r of a warpgroup owns row r of its tile (TMEM lane r): scores
-//    are masked by key index (causal and length) on boundary tiles only, reduced with tree
-//    max/sum, the running max is only moved when it grows by more than 2^8 (then O is
-//    rescaled in tensor memory), and p = 2^(s*scale - m) comes from one packed fma per pair.
-//    Rows of the last V tile past the sequence are zeroed, so stale or poisoned rows never
-//    meet a zero probability.
-//  * Every wait is bounded; on a timeout the kernel records PA_DEV_ERR_TIMEOUT, runs to
-//    the end of its protocol and frees its tensor memory.
-#include <cuda.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-#include <math.h>
-#include <stdint.h>
-
-#include <mutex>
-
-#include "pa_device.cuh"
-#include "pa_launch.h"
-#include "umma.cuh"
+// prefill.cu — host side of pa_prefill_varlen: the 4-D tensor maps over the paged cache,
+// the supported shapes, and the launch of the prefill kernel (prefill_kernel.cuh); head_dim
+// 128 with bf16 is instantiated here, the other combinations in prefill_d*_*.cu.
+#include "prefill_kernel.cuh"
 
 namespace pa {
 namespace {
-
-constexpr int kRows = 128;                 // query rows per tile (TMEM lanes)
-constexpr int kKeys = 128;                 // keys per K/V tile
-constexpr int kKStages = 3, kVStages = 2;  // ring depths
-constexpr int kHalf = 128 * 128;           // 128 rows x 64 dims: one swizzled column block
-constexpr int kTile = 2 * kHalf;           // 128 x 128 bf16
-constexpr int kThreads = 320;              // warps 0-3 tile A, 4-7 tile B, 8 TMA, 9 MMA
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows 256x
-
-// TMEM columns: S (then P) of tile g at g*128, O of tile g at 256 + g*128.
-__host__ __device__ constexpr uint32_t col_s(int g) { return (uint32_t)(g * 128); }
-__host__ __device__ constexpr uint32_t col_o(int g) { return (uint32_t)(256 + g * 128); }
-
-struct PrefillSmem {
-  // 1024-byte aligned tiles (128-byte swizzle atoms are 1024 bytes)
-  unsigned char q[2][kTile];         // [tile]
-  unsigned char k[kKStages][kTile];  // [stage]
-  unsigned char v[kVStages][kTile];
-  uint64_t q_full;
-  uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];        // S products of that K stage done
-  uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];        // PV products of that V stage done
-  uint64_t s_full[2];                // [tile]
-  uint64_t p_full[2];
-  uint64_t o_done[2];                // the tile's last PV done
-  uint32_t tmem_base;
-  int abort;
-};
-
-__device__ __forceinline__ void note_timeout(PrefillSmem& sm, int* dev_err) {
-  sm.abort = 1;
-  set_dev_err(dev_err, PA_DEV_ERR_TIMEOUT);
-}
-
-template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-  constexpr int P = kRows / G;  // query positions per tile
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int j = blockIdx.x;  // KV head
-  const int s = blockIdx.y;  // sequence
-  const int qt = (int)gridDim.z - 1 - (int)blockIdx.z;  // heaviest (latest) tiles first
-  const int H = a.num_heads;
-
-  // ---- sequence shape (uniform over the CTA) ------------------------------------------
-  const int q0 = __ldg(a.cu_seqlens_q + s);
-  const int n = __ldg(a.cu_seqlens_q + s + 1) - q0;
-  const int kv_len = __ldg(a.cu_seqlens_k + s + 1) - __ldg(a.cu_seqlens_k + s);
-  const int c_len = kv_len - n;
-  const int cap = a.max_blocks * a.block_size;
-  if (n < 0 || c_len < 0 || kv_len > cap) {
-    if (tid == 0 && qt == 0 && j == 0) set_dev_err(a.dev_err, PA_DEV_ERR_SEQLENS);
-    return;
-  }
-  if (n > a.max_seqlen_q && tid == 0 && qt == 0 && j == 0) set_dev_err(a.dev_err, PA_DEV_ERR_SEQLENS);
-  const int i0 = qt * 2 * P;
-  if (i0 >= n) return;  // nothing to do (before any barrier or tensor memory)
-  // keys needed by each tile (causal: up to its last position); tile B may be empty
-  int n_tiles[2];
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const int rows = min(P, n - (i0 + g * P));
-    const int keys = rows <= 0 ? 0 : (a.causal ? c_len + i0 + g * P + rows : kv_len);
-    n_tiles[g] = (keys + kKeys - 1) / kKeys;
-  }
-  const int n_all = max(n_tiles[0], n_tiles[1]);
-
-  if (tid == 0) {
-    mbar_init(&sm.q_full, 2 * kRows);
-    for (int b = 0; b < kKStages; ++b) {
-      mbar_init(&sm.k_full[b], 1);
-      mbar_init(&sm.k_empty[b], 1);
-    }
-    for (int b = 0; b < kVStages; ++b) {
-      mbar_init(&sm.v_full[b], 1);
-      mbar_init(&sm.v_empty[b], 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(&sm.s_full[g], 1);
-      mbar_init(&sm.p_full[g], kRows);
-      mbar_init(&sm.o_done[g], 1);
-    }
-    sm.abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == kMmaWarp) {
-    umma::tmem_alloc(&sm.tmem_base, kTmemCols);
-    umma::tmem_relinquish();
-  }
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  const uint32_t tmem = sm.tmem_base;
-  volatile int* abort_flag = &sm.abort;
-
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      umma::prefetch_tmap(&tm_k);
-      umma::prefetch_tmap(&tm_v);
-      const int bs = a.block_size;
-      const int box_rows = bs < kKeys ? bs : kKeys;
-      const int boxes = kKeys / box_rows;
-      const int32_t* table = a.block_tables + (int64_t)s * a.max_blocks;
-      auto load = [&](bool is_v, int it) {
-        const int stages = is_v ? kVStages : kKStages;
-        const int st = it % stages;
-        uint64_t* empty = is_v ? &sm.v_empty[st] : &sm.k_empty[st];
-        uint64_t* full = is_v ? &sm.v_full[st] : &sm.k_full[st];
-        if (it >= stages && !mbar_wait(empty, (uint32_t)(((it / stages) - 1) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
-        const int t0 = it * kKeys;
-        int blk[kKeys / 8];  // at most 16 boxes (block_size 8)
-        uint32_t bytes = 0;
-        for (int bx = 0; bx < boxes; ++bx) {
-          const int key0 = t0 + bx * box_rows;
-          blk[bx] = -1;
-          if (key0 < kv_len) {
-            const int id = __ldg(table + key0 / bs);
-            if (id >= 0 && (int64_t)id < a.num_blocks) {
-              blk[bx] = id;
-              bytes += 2u * box_rows * 128u;
-            } else if (!is_v) {
-              set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
-            }
-          }
-        }
-        const int row0 = (bs > kKeys) ? (t0 % bs) : 0;
-        unsigned char* dst = is_v ? sm.v[st] : sm.k[st];
-        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-        mbar_arrive_expect_tx(full, bytes);
-        for (int bx = 0; bx < boxes; ++bx) {
-          if (blk[bx] < 0) continue;
-          for (int h2 = 0; h2 < 2; ++h2)
-            umma::tma_load_4d(dst + h2 * kHalf + bx * box_rows * 128, map, h2 * 64, j, row0,
-                              blk[bx], full);
-        }
-      };
-      // K runs one tile ahead of V: S(i+1) is issued right after PV(i)
-      load(false, 0);
-      for (int it = 0; it < n_all; ++it) {
-        load(true, it);
-        if (it + 1 < n_all) load(false, it + 1);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = umma::idesc_bf16_f32(kRows, kKeys, false);
-      constexpr uint32_t idesc_o = umma::idesc_bf16_f32(kRows, 128, true);
-      auto issue_s = [&](int g, int it) {  // S_g = Q_g K(it)^T
-        const uint32_t k_addr = smem_u32(sm.k[it % kKStages]);
-        const uint32_t q_addr = smem_u32(sm.q[g]);
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma::mma_bf16(tmem + col_s(g), umma::smem_desc(q_addr + off, 16, 1024),
-                         umma::smem_desc(k_addr + off, 16, 1024), idesc_s, kk > 0);
-        }
-        umma::commit(&sm.s_full[g]);
-      };
-      auto issue_pv = [&](int g, int it) {  // O_g += P_g V(it), P_g read from tensor memory
-        const uint32_t v_addr = smem_u32(sm.v[it % kVStages]);
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma::mma_bf16_ts(tmem + col_o(g), tmem + col_s(g) + kk * 8,
-                            umma::smem_desc(v_addr + kk * 16 * 128, kHalf, 1024), idesc_o,
-                            (it > 0) || (kk > 0));
-        if (it == n_tiles[g] - 1) umma::commit(&sm.o_done[g]);
-      };
-      auto wait_k = [&](int it) {
-        if (!mbar_wait(&sm.k_full[it % kKStages], (uint32_t)((it / kKStages) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
-        umma::fence_after_sync();
-      };
-      if (!mbar_wait(&sm.q_full, 0, abort_flag)) note_timeout(sm, a.dev_err);
-      umma::fence_after_sync();
-      wait_k(0);
-#pragma unroll
-      for (int g = 0; g < 2; ++g)
-        if (n_tiles[g] > 0) issue_s(g, 0);
-      umma::commit(&sm.k_empty[0]);
-      for (int it = 0; it < n_all; ++it) {
-        bool v_ready = false, k_ready = false;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          if (it >= n_tiles[g]) continue;
-          if (!mbar_wait(&sm.p_full[g], (uint32_t)(it & 1), abort_flag)) note_timeout(sm, a.dev_err);
-          if (!v_ready) {
-            if (!mbar_wait(&sm.v_full[it % kVStages], (uint32_t)((it / kVStages) & 1), abort_flag))
-              note_timeout(sm, a.dev_err);
-            v_ready = true;
-          }
-          umma::fence_after_sync();
-          issue_pv(g, it);
-          if (it + 1 < n_tiles[g]) {
-            if (!k_ready) {
-              wait_k(it + 1);
-              k_ready = true;
-            }
-            issue_s(g, it + 1);
-          }
-        }
-        umma::commit(&sm.v_empty[it % kVStages]);
-        if (k_ready) umma::commit(&sm.k_empty[(it + 1) % kKStages]);
-      }
-      // the last products must land before tensor memory is released
-#pragma unroll
-      for (int g = 0; g < 2; ++g)
-        if (n_tiles[g] > 0 && !mbar_wait(&sm.o_done[g], 0, abort_flag)) note_timeout(sm, a.dev_err);
-    }
-  } else {
-    // ------------------------------------------------------------------ softmax warpgroups
-    const int g = warp >> 2;      // query tile of this warpgroup
-    const int r = tid & 127;      // row == TMEM lane
-    const int wq = warp & 3;      // warp within the warpgroup (TMEM lane quarter)
-    const int pos = r / G, hh = r % G;
-    const int qi = i0 + g * P + pos;     // new-token index within the sequence
-    const bool row_ok = qi < n;
-    const int qpos = c_len + qi;         // absolute position of this query row
-    const int lim_row = a.causal ? min(kv_len, qpos + 1) : kv_len;  // keys [0, lim_row) count
-    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const int nt = n_tiles[g];
-
-    // Q row -> shared memory (128-byte swizzled, K-major)
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const uint16_t*>(a.q) + ((int64_t)(q0 + qi) * H + j * G + hh) * kHeadDim);
-      uint4 qv[16];
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) qv[ch] = row_ok ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch)
-        *reinterpret_cast<uint4*>(sm.q[g] + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
-            qv[ch];
-      fence_proxy_async_smem();
-      mbar_arrive(&sm.q_full);
-    }
-
-    float m_run = -INFINITY, l_run = 0.f;
-    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-    for (int it = 0; it < nt; ++it) {
-      if (!mbar_wait(&sm.s_full[g], (uint32_t)(it & 1), abort_flag)) note_timeout(sm, a.dev_err);
-      umma::fence_after_sync();
-      float sv[kKeys];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) umma::tmem_ld32(lane_addr + col_s(g) + 32 * c4, sv + 32 * c4);
-      umma::tmem_ld_wait();
-
-      const int t0 = it * kKeys;
-      // only tiles that reach past this row's last visible key need a mask
-      if (__any_sync(0xffffffffu, t0 + kKeys > lim_row)) {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c)
-          if (t0 + c >= lim_row) sv[c] = -INFINITY;
-      }
-      float mx[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) mx[c] = sv[c];
-#pragma unroll
-      for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-      // the scale is positive, so the max of the scaled scores is the scaled max
-      const float mt = a.scale_log2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                            fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      float m_use, alpha;
-      bool rescale = false;
-      if (it == 0) {
-        m_use = mt;
-        alpha = 0.f;
-      } else if (mt > m_run + kRescaleThreshold) {
-        m_use = mt;
-        alpha = fast_exp2(m_run - mt);
-        rescale = true;
-      } else {
-        m_use = m_run;
-        alpha = 1.f;
-      }
-      const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
-      // p = 2^(s*scale - m): one packed fma per pair, then ex2; P packed as bf16 pairs over S
-      const float2 nm2 = make_float2(-m_safe, -m_safe);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < kKeys / 2; ++c) {
-        const float2 x = umma::ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sc2, nm2);
-        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-        acc[c & 3] = umma::fadd2(acc[c & 3], p);
-        sv[c] = __uint_as_float(f32x2_to_bf16x2(p.x, p.y));  // c <= 2c: in place is safe
-      }
-      const float2 t01 = umma::fadd2(acc[0], acc[1]), t23 = umma::fadd2(acc[2], acc[3]);
-      const float2 tt = umma::fadd2(t01, t23);
-      l_run = l_run * alpha + (tt.x + tt.y);
-      m_run = m_use;
-      umma::tmem_st32(lane_addr + col_s(g), sv);
-      umma::tmem_st32(lane_addr + col_s(g) + 32, sv + 32);
-      // O_g is stable here (S_g(it) completed after PV_g(it-1)); PV_g(it) waits for p_full
-      if (__any_sync(0xffffffffu, rescale)) {
-        float ob[32];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob);
-          umma::tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ob[e] *= alpha;
-          umma::tmem_st32(lane_addr + col_o(g) + 32 * c4, ob);
-        }
-      }
-      // rows of the last V tile beyond the sequence: zero them (never multiply a stale row)
-      if (t0 + kKeys > kv_len) {
-        const int st = it % kVStages;
-        if (!mbar_wait(&sm.v_full[st], (uint32_t)((it / kVStages) & 1), abort_flag))
-          note_timeout(sm, a.dev_err);
-        const int first_bad = kv_len - t0;
-        if (r >= first_bad) {
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch)
-            *reinterpret_cast<uint4*>(sm.v[st] + (ch >> 3) * kHalf + r * 128 + (ch & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-      }
-      umma::tmem_st_wait();
-      umma::fence_before_sync();
-      mbar_arrive(&sm.p_full[g]);
-    }
-
-    // ---- epilogue: O / l -> bf16 rows ------------------------------------------------
-    if (nt > 0) {
-      if (!mbar_wait(&sm.o_done[g], 0, abort_flag)) note_timeout(sm, a.dev_err);
-      umma::fence_after_sync();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                            ((int64_t)(q0 + qi) * H + j * G + hh) * kHeadDim);
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float ob[32];
-        umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob);
-        umma::tmem_ld_wait();
-        if (row_ok) {
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 pk;
-            pk.x = f32x2_to_bf16x2(ob[8 * q8 + 0] * inv, ob[8 * q8 + 1] * inv);
-            pk.y = f32x2_to_bf16x2(ob[8 * q8 + 2] * inv, ob[8 * q8 + 3] * inv);
-            pk.z = f32x2_to_bf16x2(ob[8 * q8 + 4] * inv, ob[8 * q8 + 5] * inv);
-            pk.w = f32x2_to_bf16x2(ob[8 * q8 + 6] * inv, ob[8 * q8 + 7] * inv);
-            dst[c4 * 4 + q8] = pk;
-          }
-        }
-      }
-    }
-  }
-
-  // ---- teardown: every role is done with tensor memory ----------------------------------
-  umma::fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    umma::fence_after_sync();
-    umma::tmem_dealloc(tmem, kTmemCols);
-  }
-}
 
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -435,43 +21,23 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int block_size,
-                    int64_t num_blocks) {
+bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int head_dim,
+                    bool f16, int block_size, int64_t num_blocks) {
   auto encode = get_encode();
   if (!encode) return false;
   const int box_rows = block_size < kKeys ? block_size : kKeys;
-  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+  cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
                         (cuuint64_t)num_blocks};
-  cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)num_kv_heads * kHeadDim * 2,
-                           (cuuint64_t)block_size * num_kv_heads * kHeadDim * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_kv_heads * head_dim * 2,
+                           (cuuint64_t)block_size * num_kv_heads * head_dim * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult rc = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+  CUresult rc = encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                       4, const_cast<void*>(base), dims,
                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS;
-}
-
-template <int G>
-int launch_prefill_t(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream,
-                     const CUtensorMap& mk, const CUtensorMap& mv) {
-  constexpr int P = kRows / G;
-  const size_t smem = sizeof(PrefillSmem) + 1024;
-  static_assert(sizeof(PrefillSmem) + 1024 <= 227 * 1024, "shared memory budget");
-  static bool attr_done[64] = {false};
-  if (info.device < 0 || info.device >= 64) return PA_ERR_CUDA;
-  if (!attr_done[info.device]) {
-    if (cudaFuncSetAttribute(paged_prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_done[info.device] = true;
-  }
-  const int q_tiles = (a.max_seqlen_q + 2 * P - 1) / (2 * P);  // pairs of query tiles
-  if (q_tiles > 65535) return PA_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)a.num_kv_heads, (unsigned)a.num_seqs, (unsigned)q_tiles);
-  paged_prefill_kernel<G><<<grid, kThreads, smem, stream>>>(mk, mv, a);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -487,16 +53,16 @@ bool prefill_supported(int num_heads, int num_kv_heads, int block_size) {
 int launch_prefill(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream) {
   if (a.num_seqs > 65535 || a.max_seqlen_q <= 0) return PA_ERR_UNSUPPORTED;
   CUtensorMap mk, mv;
-  if (!make_cache_map(&mk, a.k_cache, a.num_kv_heads, a.block_size, a.num_blocks) ||
-      !make_cache_map(&mv, a.v_cache, a.num_kv_heads, a.block_size, a.num_blocks))
+  if (!make_cache_map(&mk, a.k_cache, a.num_kv_heads, a.head_dim, a.f16, a.block_size,
+                      a.num_blocks) ||
+      !make_cache_map(&mv, a.v_cache, a.num_kv_heads, a.head_dim, a.f16, a.block_size,
+                      a.num_blocks))
     return PA_ERR_CUDA;
-  switch (a.num_heads / a.num_kv_heads) {
-    case 1: return launch_prefill_t<1>(a, info, stream, mk, mv);
-    case 2: return launch_prefill_t<2>(a, info, stream, mk, mv);
-    case 4: return launch_prefill_t<4>(a, info, stream, mk, mv);
-    case 8: return launch_prefill_t<8>(a, info, stream, mk, mv);
-    default: return PA_ERR_UNSUPPORTED;
-  }
+  if (a.head_dim == 128 && !a.f16) return dispatch_prefill<128, false>(a, info, stream, mk, mv);
+  if (a.head_dim == 64) return a.f16 ? launch_prefill_d64_f16(a, info, stream, mk, mv)
+                                     : launch_prefill_d64_bf16(a, info, stream, mk, mv);
+  if (a.head_dim == 128) return launch_prefill_d128_f16(a, info, stream, mk, mv);
+  return PA_ERR_UNSUPPORTED;
 }
 
 }  // namespace pa

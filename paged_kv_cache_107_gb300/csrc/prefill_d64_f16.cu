@@ -1,0 +1,12 @@
+// prefill_d64_f16.cu — instantiation of the prefill kernel (prefill_kernel.cuh) for head_dim 64
+// with IEEE fp16 elements, in its own translation unit so the variants compile in parallel.
+#include "prefill_kernel.cuh"
+
+namespace pa {
+
+int launch_prefill_d64_f16(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t stream,
+                   const CUtensorMap& mk, const CUtensorMap& mv) {
+  return dispatch_prefill<64, true>(a, info, stream, mk, mv);
+}
+
+}  // namespace pa

@@ -269,10 +269,17 @@ WORKLOADS = {
 
 
 def workload(num: int, block_size: Optional[int] = None, poison: bool = True,
-             num_blocks: Optional[int] = None) -> PagedCase:
+             num_blocks: Optional[int] = None, head_dim: int = 128,
+             dtype: torch.dtype = torch.bfloat16) -> PagedCase:
     """Build named workload `num` (1..5). Workload 4 takes block_size 16 or 256.
     num_blocks overrides the pool size of workloads 2, 3 and 5 (the drawn lengths and the
-    values do not change; only the physical ids do)."""
+    values do not change; only the physical ids do). head_dim (64 or 128) and the element
+    type (bf16 or fp16) apply to workloads 2 and 5: the same lengths and block tables with
+    other head sizes or element types."""
+    if (head_dim != 128 or dtype != torch.bfloat16) and num not in (2, 5):
+        raise ValueError("head_dim / dtype variants exist for workloads 2 and 5")
+    sfx = "" if (head_dim == 128 and dtype == torch.bfloat16) else \
+        f"_d{head_dim}_{'fp16' if dtype == torch.float16 else 'bf16'}"
     seed = SEED_BASE + num
     if num == 1:
         return decode_case([1, 17, 256, 300], 16, 8, 128, 256, num_blocks=16, seed=seed,
@@ -280,9 +287,9 @@ def workload(num: int, block_size: Optional[int] = None, poison: bool = True,
     rng = np.random.default_rng(seed)
     if num == 2:
         lens = rng.integers(100, 2048 + 1, size=256)
-        return decode_case(lens, 16, 8, 128, 256, num_blocks=num_blocks or 4096,
+        return decode_case(lens, 16, 8, head_dim, 256, num_blocks=num_blocks or 4096,
                            seed=seed + 1000, poison=poison, max_blocks=8,
-                           name="w2_qwen3_decode_b256")
+                           name="w2_qwen3_decode_b256" + sfx, dtype=dtype)
     if num == 3:
         lens = rng.integers(32768, 131072 + 1, size=8)
         return decode_case(lens, 32, 8, 128, 256, num_blocks=num_blocks or 4096,
@@ -298,7 +305,7 @@ def workload(num: int, block_size: Optional[int] = None, poison: bool = True,
     if num == 5:
         cached = rng.integers(0, 2048 + 1, size=32)
         new = rng.integers(100, 1024 + 1, size=32)
-        return prefill_case(cached, new, 16, 8, 128, 256, num_blocks=num_blocks or 4096,
+        return prefill_case(cached, new, 16, 8, head_dim, 256, num_blocks=num_blocks or 4096,
                             seed=seed + 1000, poison=poison, causal=True,
-                            name="w5_chunked_prefill")
+                            name="w5_chunked_prefill" + sfx, dtype=dtype)
     raise ValueError(f"no workload {num}")

@@ -15,8 +15,8 @@ def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def from_bits(a):
-    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+def from_bits(a, dtype=torch.bfloat16):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dtype)
 
 
 class DeviceCase:

@@ -55,11 +55,14 @@ def test_validation_without_launch(lib):
     lib.pa_decode.restype = ctypes.c_int
     vp = ctypes.c_void_p(16)
     # H % Hk != 0
-    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 12, 8, 128, 16, ctypes.c_int64(4),
+    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 12, 8, 128, 1, 16, ctypes.c_int64(4),
                        ctypes.c_float(0), 0, vp, ctypes.c_size_t(1 << 20), None, None)
     assert rc == 2
-    # head_dim 64
-    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 16, 8, 64, 16, ctypes.c_int64(4),
+    # head_dim 96; element type F32 (not an attention type)
+    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 16, 8, 96, 1, 16, ctypes.c_int64(4),
+                       ctypes.c_float(0), 0, vp, ctypes.c_size_t(1 << 20), None, None)
+    assert rc == 3
+    rc = lib.pa_decode(vp, vp, vp, vp, vp, 1, vp, 2, 16, 8, 64, 0, 16, ctypes.c_int64(4),
                        ctypes.c_float(0), 0, vp, ctypes.c_size_t(1 << 20), None, None)
     assert rc == 3
     # store: negative token count, bad stride
@@ -80,10 +83,10 @@ def test_validation_without_launch(lib):
 
     def step(kstride, head_dim, B):
         return lib.pa_decode_step(vp, vp, vp, vp, i64(kstride), i64(1024), vp, vp, vp, vp, 1, vp,
-                                  B, 16, 8, head_dim, 16, i64(4), ctypes.c_float(0), 0, vp,
+                                  B, 16, 8, head_dim, 1, 16, i64(4), ctypes.c_float(0), 0, vp,
                                   ctypes.c_size_t(1 << 20), None, None)
     assert step(1000, 128, 2) == 2
-    assert step(1024, 64, 2) == 3
+    assert step(1024, 32, 2) == 3
     assert step(1024, 128, 0) == 0
     # sampler: row stride below the vocabulary, unknown dtype, zero rows
     lib.pa_gumbel_sample.restype = ctypes.c_int
@@ -98,6 +101,6 @@ def test_validation_without_launch(lib):
     assert lib.pa_sample_workspace_size(-1) == 0 and lib.pa_sample_workspace_size(256) >= 256 * 12
     # prefill: max_seqlen_k beyond what the table maps
     lib.pa_prefill_varlen.restype = ctypes.c_int
-    rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 256,
+    rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 1, 256,
                                ctypes.c_int64(4), 1, ctypes.c_float(0), None, None)
     assert rc in (2, 3)

@@ -168,11 +168,11 @@ def test_host_validation_launches_nothing():
         pk.pa_decode(out, q, kc, kc, bt, ctx, workspace=small)
     with pytest.raises(pk.PagedAttentionError, match="SHAPE"):
         pk.pa_decode(out, q, kc, kc, bt, ctx, grid_ctas=100000)
-    q64 = torch.zeros((2, 16, 64), dtype=torch.bfloat16, device=dev)
-    kc64 = torch.zeros((4, 16, 8, 64), dtype=torch.bfloat16, device=dev)
+    q96 = torch.zeros((2, 16, 96), dtype=torch.bfloat16, device=dev)
+    kc96 = torch.zeros((4, 16, 8, 96), dtype=torch.bfloat16, device=dev)
     ws = pk.DecodeWorkspace(2, 16, 8)
-    with pytest.raises(pk.PagedAttentionError, match="UNSUPPORTED"):
-        pk.pa_decode(torch.zeros_like(q64), q64, kc64, kc64, bt, ctx, workspace=ws)
+    with pytest.raises(pk.PagedAttentionError, match="UNSUPPORTED"):  # head_dim 96
+        pk.pa_decode(torch.zeros_like(q96), q96, kc96, kc96, bt, ctx, workspace=ws)
 
 
 @pytest.mark.parametrize("num", [2, 3])

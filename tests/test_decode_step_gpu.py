@@ -169,7 +169,7 @@ def test_rejects_bad_arguments():
         return lib.pa_decode_step(
             a["out"].data_ptr(), a["q"].data_ptr(), a["kn"], a["vn"], a["ks"], a["vs"],
             dc.k_cache.data_ptr(), dc.v_cache.data_ptr(), dc.slots.data_ptr(),
-            dc.bt.data_ptr(), 2, dc.ctx.data_ptr(), 4, 16, 8, 128, 256, 16, 0.0, 0,
+            dc.bt.data_ptr(), 2, dc.ctx.data_ptr(), 4, 16, 8, 128, 1, 256, 16, 0.0, 0,
             ws.buffer.data_ptr(), ws.nbytes, None, None)
 
     kn, vn = dc.k_new.data_ptr(), dc.v_new.data_ptr()
