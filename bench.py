@@ -59,7 +59,7 @@ def source_sha256(*names) -> str:
 
 
 DECODE_SOURCES = ("decode_kernel.cuh", "pa_device.cuh")
-PREFILL_SOURCES = ("prefill.cu", "umma.cuh", "pa_device.cuh")
+PREFILL_SOURCES = ("prefill_kernel.cuh", "prefill.cu", "umma.cuh", "pa_device.cuh")
 
 
 def profile_value(sources, summary: str, key: str):
@@ -383,13 +383,20 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128
     _, tflops_peak, src = measured_peaks()
     nq = int(case.cu_seqlens_q[-1])
     store_bytes = nq * case.num_kv_heads * case.head_dim * 2 * 2 * 2
-    return {"workload": case.name, "new_tokens": nq, "flops": flops,
-            "prefill_ms": pf_ms, "store_ms": st_ms,
-            "tflops": flops / (pf_ms * 1e-3) / 1e12,
-            "tflops_frac": flops / (pf_ms * 1e-3) / 1e12 / tflops_peak,
-            "peak_tflops": tflops_peak, "peak_source": f"{src} bf16 dense (sustained)",
-            "tokens_per_s": nq / (pf_ms * 1e-3),
-            "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
+    res = {"workload": case.name, "new_tokens": nq, "flops": flops,
+           "prefill_ms": pf_ms, "store_ms": st_ms,
+           "tflops": flops / (pf_ms * 1e-3) / 1e12,
+           "tflops_frac": flops / (pf_ms * 1e-3) / 1e12 / tflops_peak,
+           "peak_tflops": tflops_peak, "peak_source": f"{src} bf16 dense (sustained)",
+           "tokens_per_s": nq / (pf_ms * 1e-3),
+           "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
+    if head_dim == 128 and (dtype is None or dtype == torch.bfloat16):
+        res["roofline"] = {
+            "kernel": "paged_prefill_kernel", "bound": "tensor", "unit": "TFLOP/s",
+            "achieved": res["tflops"], "peak": tflops_peak, "frac": res["tflops_frac"],
+            "peak_source": f"{src} cuBLAS bf16 dense, sustained",
+            "traffic": kernel_traffic(PREFILL_SOURCES, "prefill_w5_chunked.md")}
+    return res
 
 
 def measure_variants(dev, steps: int, warmup: int):
