@@ -692,23 +692,26 @@ def run_ours(args):
     traffic = kernel_traffic(DECODE_SOURCES + ("decode_step.cu",), "decode_step_w2_qwen3_b256.md")
 
     # ---- end to end through the public API with host buffers ---------------------------
-    pin = lambda t: t.pin_memory()
-    h_q, h_k, h_v = pin(case.q), pin(case.k_new), pin(case.v_new)
-    h_slots = pin(torch.from_numpy(case.slot_mapping))
-    h_bt = pin(torch.from_numpy(case.block_tables))
-    h_ctx = pin(torch.from_numpy(case.context_lens))
+    # the step's inputs sit in one pinned host buffer (DecodeStepBuffers) and move with one
+    # copy; the device views go to pa_decode_step; the output comes back with one copy
+    from paged_kv_cache_107_gb300.step_io import DecodeStepBuffers
+    io = DecodeStepBuffers(B, H, Hk, D, case.block_tables.shape[1], dtype=q.dtype, device=dev)
+    io.host["q"].copy_(case.q)
+    io.host["k_new"].copy_(case.k_new)
+    io.host["v_new"].copy_(case.v_new)
+    io.host["slot_mapping"].copy_(torch.from_numpy(case.slot_mapping))
+    io.host["block_tables"].copy_(torch.from_numpy(case.block_tables))
+    io.host["context_lens"].copy_(torch.from_numpy(case.context_lens))
+    d = io.dev
     h_out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_ctx))
+    h2d = io.nbytes
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        q.copy_(h_q, non_blocking=True)
-        k_new.copy_(h_k, non_blocking=True)
-        v_new.copy_(h_v, non_blocking=True)
-        slots.copy_(h_slots, non_blocking=True)
-        bt.copy_(h_bt, non_blocking=True)
-        ctx.copy_(h_ctx, non_blocking=True)
-        step()
+        io.upload(stream)
+        pk.pa_decode_step(out, d["q"], d["k_new"], d["v_new"], k_cache, v_cache, d["slot_mapping"],
+                          d["block_tables"], d["context_lens"], workspace=ws, dev_err=err,
+                          stream=stream)
         h_out.copy_(out, non_blocking=True)
 
     for _ in range(3):

@@ -179,3 +179,30 @@ def test_rejects_bad_arguments():
     assert call(kn=kn, vn=vn, ks=8 * 128 + 4) == 6   # PA_ERR_ALIGN (stride)
     assert call(kn=kn, vn=vn, vs=100) == 2           # PA_ERR_SHAPE (stride below a row)
     torch.cuda.synchronize()
+
+
+def test_step_on_packed_buffers_equals_separate_tensors():
+    """The step's inputs staged in one pinned buffer and moved with one copy
+    (DecodeStepBuffers): the fused step on those device views gives the same bits."""
+    from paged_kv_cache_107_gb300.step_io import DecodeStepBuffers
+    case = workloads.decode_case([5, 260, 1, 999, 0, 77], 16, 8, 128, 256, seed=1800)
+    ref_dc = DeviceCase(case)
+    ref = fused(ref_dc)
+    io = DecodeStepBuffers(6, 16, 8, 128, case.block_tables.shape[1])
+    io.host["q"].copy_(case.q)
+    io.host["k_new"].copy_(case.k_new)
+    io.host["v_new"].copy_(case.v_new)
+    io.host["slot_mapping"].copy_(torch.from_numpy(case.slot_mapping))
+    io.host["block_tables"].copy_(torch.from_numpy(case.block_tables))
+    io.host["context_lens"].copy_(torch.from_numpy(case.context_lens))
+    io.upload()
+    kc, vc = case.k_cache.cuda(), case.v_cache.cuda()
+    out = torch.full_like(ref, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = io.dev
+    pk.pa_decode_step(out, d["q"], d["k_new"], d["v_new"], kc, vc, d["slot_mapping"],
+                      d["block_tables"], d["context_lens"], dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and ref_dc.dev_err() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), ref_dc.k_cache.view(torch.int16))
