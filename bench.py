@@ -401,15 +401,23 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128
 
 def measure_variants(dev, steps: int, warmup: int):
     """head_dim 64 / IEEE fp16 variants on the shapes of the decode step (workload 2: the
-    fused store + decode, one launch) and of the chunked prefill (workload 5)."""
+    fused store + decode, one launch) and of the chunked prefill (workload 5); and the
+    decode step with 4 and 8 query heads per KV head (the tensor-core path)."""
     import torch
     import paged_kv_cache_107_gb300 as pk
     from paged_kv_cache_107_gb300 import workloads
     hbm_peak, _, peak_src = measured_peaks()
     res = {"peak_gbs": hbm_peak, "peak_source": f"{peak_src} HBM copy GB/s"}
-    for D, dt, tag in ((64, torch.bfloat16, "d64_bf16"), (64, torch.float16, "d64_fp16"),
-                       (128, torch.float16, "d128_fp16")):
-        case = workloads.workload(2, poison=True, head_dim=D, dtype=dt)
+    for D, dt, tag, heads in ((64, torch.bfloat16, "d64_bf16", 16), (64, torch.float16, "d64_fp16", 16),
+                              (128, torch.float16, "d128_fp16", 16), (128, torch.bfloat16, "g4", 32),
+                              (128, torch.bfloat16, "g8", 64)):
+        if heads == 16:
+            case = workloads.workload(2, poison=True, head_dim=D, dtype=dt)
+        else:  # the same lengths and tables with 4 or 8 query heads per KV head
+            base = workloads.workload(2, poison=False)
+            case = workloads.decode_case(base.context_lens, heads, 8, D, 256, num_blocks=4096,
+                                         seed=107002 + 1000, poison=True, max_blocks=8,
+                                         name=f"w2_decode_b256_h{heads}_hk8", dtype=dt)
         tot_ctx, kv_bytes, small_bytes, store_bytes = workload_summary(case)
         kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
         q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
@@ -445,8 +453,9 @@ def measure_variants(dev, steps: int, warmup: int):
             "achieved_gbs": alg / (ms * 1e-3) / 1e9,
             "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak}
         del kc, vc, case
-        res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
-                                                head_dim=D, dtype=dt)
+        if heads == 16:
+            res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
+                                                    head_dim=D, dtype=dt)
     return res
 
 

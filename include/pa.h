@@ -27,7 +27,8 @@
  *   - Layouts are C-contiguous unless a stride argument says otherwise:
  *       k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim]
  *       block_tables      [num_seqs, max_blocks_per_seq] int32, right-padded with -1
- *   - GQA: query head h reads KV head h / (num_heads / num_kv_heads).
+ *   - GQA: query head h reads KV head h / (num_heads / num_kv_heads). Decode (and the fused
+ *     step) take 1 to 8 query heads per KV head; prefill takes 1, 2, 4 or 8.
  *   - Host-side validation happens before any launch; when it fails the call returns
  *     the status and launches nothing.
  *   - Data-dependent errors that only the device can see (a block id outside

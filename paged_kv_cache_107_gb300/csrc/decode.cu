@@ -15,7 +15,7 @@ int decode_head_slab(int num_kv_heads) {
 bool decode_supported(int num_heads, int num_kv_heads) {
   if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return false;
   const int g = num_heads / num_kv_heads;
-  return g == 1 || g == 2 || g == 4 || g == 8;
+  return g >= 1 && g <= 8;  // 1, 2 on CUDA cores; 3..8 on the tensor-core path
 }
 
 int decode_max_ctas(const DeviceInfo& info) { return 4 * info.num_sms; }
@@ -37,6 +37,7 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
 }
 
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
+  if (decode_uses_tc(a.num_heads, a.num_kv_heads)) return launch_decode_tc(a, info, stream);
   if (a.head_dim == 128 && !a.f16) return dispatch_slab<false, 128, false>(a, info, stream);
   if (a.head_dim == 64) return a.f16 ? launch_decode_d64_f16(a, info, stream)
                                      : launch_decode_d64_bf16(a, info, stream);

@@ -1,0 +1,15 @@
+// decode_tc.cu — instantiations of the decode on the tensor-core path (decode_tc.cuh): query-head
+// groups of 3 to 8 per KV head, head_dim 64 or 128, bf16 or IEEE fp16 elements.
+#include "decode_tc.cuh"
+
+namespace pa {
+
+int launch_decode_tc(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
+  if (a.head_dim == 128) return a.f16 ? dispatch_slab_tc<false, 128, true>(a, info, stream)
+                                      : dispatch_slab_tc<false, 128, false>(a, info, stream);
+  if (a.head_dim == 64) return a.f16 ? dispatch_slab_tc<false, 64, true>(a, info, stream)
+                                     : dispatch_slab_tc<false, 64, false>(a, info, stream);
+  return PA_ERR_UNSUPPORTED;
+}
+
+}  // namespace pa

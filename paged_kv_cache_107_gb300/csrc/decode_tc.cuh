@@ -1,0 +1,652 @@
+// decode_tc.cuh — paged decode attention for query-head groups of 3 to 8 per KV head on
+// the tensor cores (warp-level mma.sync m16n8k16, bf16 or fp16 operands, fp32 accumulators).
+//
+// Same computation and same work split as decode_kernel.cuh ("nano-vllm解读", sections
+// "PageAttention原理" and "Nano-vllm中的使用"; stream-K over key tiles, partials combined in
+// CTA order by the last CTA of a sequence). With G query heads per KV head the per-head work
+// is a small dense product: S = Q_j K^T (G x T) and O += P V (G x D). On CUDA cores its dot
+// products, reductions and accumulations outgrow the instruction budget of the HBM stream
+// once G >= 4 (and G = 8 no longer fits in registers); here one warp runs them as
+// 16-row tensor-core products, the G heads padded to 16 rows.
+//
+//  * Token rows of the slab land in shared memory at a stride of row + 16 bytes (one bulk
+//    copy per token row), so the 8 rows an ldmatrix reads sit in 8 different bank groups.
+//  * Warp (j, w): KV head j of the slab, tokens 16w..16w+15 of each tile. S: for every
+//    16-dim chunk, ldmatrix.x4 gives the K fragments of two 8-token column tiles; Q
+//    fragments are loaded once per sequence. Online softmax in the accumulator layout (a
+//    row's 16 scores sit in one quad of lanes); the S accumulators become the A operand of
+//    O += P V directly; V fragments come from ldmatrix.x4.trans. Rows of V past the context
+//    are zeroed first, so no stale value meets a zero probability.
+#pragma once
+
+#include "decode_kernel.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTcGMax = 8;   // query heads per KV head on this path (rows of the 16-row tile)
+constexpr int kTcStages = 2;
+
+template <int HS, int D>
+struct TcCfg {
+  static constexpr int T = 128 / HS;               // tokens per stage (8 warps x 16 / HS)
+  static constexpr int WPH = kConsumerWarps / HS;  // warps per KV head (token split)
+  static constexpr int ROW = HS * D * 2;           // bytes of one token row of the slab
+  static constexpr int RS = ROW + 16;              // its stride in shared memory
+  static constexpr int KV_BYTES = T * RS;
+  static constexpr int Q_BYTES = HS * kTcGMax * D * 2;
+  static constexpr int STAGE_BYTES = ((2 * KV_BYTES + Q_BYTES) + 127) / 128 * 128;
+  static constexpr int MERGE_FLOATS = kTcGMax * (D + 2);
+  static constexpr size_t SMEM = (size_t)kTcStages * STAGE_BYTES + 4096 + 128;
+  static_assert(HS * (WPH - 1) * MERGE_FLOATS * 4 <= 2 * KV_BYTES, "merge scratch");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+// D (16x8) += A (16x16) B (16x8) with rows 8..15 of A zero (at most 8 heads per group):
+// a0/a2 are this thread's A words of row gid, c0/c1 its accumulators of row gid; the
+// accumulators of rows 8..15 go to the scratch pair z (written, never read).
+template <bool F16>
+__device__ __forceinline__ void mma16816(float& c0, float& c1, float2& z, uint32_t a0, uint32_t a2,
+                                         uint32_t b0, uint32_t b1) {
+  const uint32_t zero = 0u;
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c0), "+f"(c1), "+f"(z.x), "+f"(z.y)
+        : "r"(a0), "r"(zero), "r"(a2), "r"(zero), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c0), "+f"(c1), "+f"(z.x), "+f"(z.y)
+        : "r"(a0), "r"(zero), "r"(a2), "r"(zero), "r"(b0), "r"(b1));
+  }
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+template <int HS, bool FUSED, int D, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const DecodeArgs a) {
+  using TC = TcCfg<HS, D>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + (size_t)kTcStages * TC::STAGE_BYTES);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int c = blockIdx.x;
+  const int slab = blockIdx.y;
+  const int H = a.num_heads;
+  const int Hk = a.num_kv_heads;
+  const int G = H / Hk;  // 3..8 on this path
+  const int cap = a.max_blocks * a.block_size;
+  const int B = a.num_seqs;
+  constexpr int T = TC::T;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&ctl.full[s], 1);
+      mbar_init(&ctl.empty[s], kConsumerWarps);
+    }
+    mbar_init(&ctl.seg_bar, kConsumerWarps);
+    if (TC::WPH > 1)
+      for (int j = 0; j < HS; ++j) mbar_init(&ctl.merge_bar[j], TC::WPH - 1);
+    ctl.found = 0;
+    ctl.abort = 0;
+    ctl.b0 = 0;
+    ctl.pb0 = 0;
+    fence_mbar_init();
+  }
+
+  // ---- prologue: total tiles, then the sequence that holds this CTA's first tile -----
+  int64_t local = 0;
+  for (int b = tid; b < B; b += kThreads) {
+    const int raw = __ldg(a.context_lens + b);
+    if (raw < 0 || raw > cap) {
+      if ((b % gridDim.x) == c && slab == 0) set_dev_err(a.dev_err, PA_DEV_ERR_CONTEXT);
+    }
+    // FUSED: a token of an empty sequence has no position to be stored at
+    if (FUSED && (raw <= 0 || raw > cap) && __ldg(a.slot_mapping + b) != -1) {
+      if ((b % gridDim.x) == c && slab == 0) set_dev_err(a.dev_err, PA_DEV_ERR_SLOT);
+    }
+    local += (load_ctx(a.context_lens, b, cap) + T - 1) / T;
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) local += __shfl_xor_sync(0xffffffffu, local, m);
+  if (lane == 0) ctl.red[warp] = local;
+  __syncthreads();
+  if (tid == 0) {
+    int64_t nt = 0;
+    for (int w = 0; w < kThreads / 32; ++w) nt += ctl.red[w];
+    ctl.nt = nt;
+    const int g_eff = (int)(nt < (int64_t)gridDim.x ? nt : (int64_t)gridDim.x);
+    ctl.g_eff = g_eff;
+    if (c < g_eff) {
+      ctl.x0 = tile_begin(c, nt, g_eff);
+      ctl.x1 = tile_begin(c + 1, nt, g_eff);
+    } else {
+      ctl.x0 = ctl.x1 = 0;
+    }
+  }
+  __syncthreads();
+  const int64_t NT = ctl.nt;
+  const int g_eff = ctl.g_eff;
+  const int64_t x0 = ctl.x0, x1 = ctl.x1;
+
+  // zero rows of empty (or invalid) sequences assigned to this CTA: one warp per row
+  {
+    const int heads_per_slab = HS * G;
+    for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
+      if (load_ctx(a.context_lens, b, cap) != 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                            ((int64_t)b * H + slab * heads_per_slab) * D);
+      const int nvec = heads_per_slab * D / 8;
+      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  if (x0 < x1) {
+    // chunked scan over the sequences until the one holding tile x0 is found
+    int64_t running = 0;
+    for (int base = 0; base < B; base += kConsumerWarps * 32) {
+      int n = 0;
+      const int b = base + tid;
+      if (tid < kConsumerWarps * 32 && b < B) n = (load_ctx(a.context_lens, b, cap) + T - 1) / T;
+      int incl = n;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, m);
+        if (lane >= m) incl += y;
+      }
+      if (lane == 31) ctl.red[warp] = incl;
+      __syncthreads();
+      int64_t warp_off = 0;
+      int64_t chunk_total = 0;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        if (w < warp) warp_off += ctl.red[w];
+        chunk_total += ctl.red[w];
+      }
+      if (tid < kConsumerWarps * 32 && b < B && n > 0) {
+        const int64_t p = running + warp_off + incl - n;
+        if (p <= x0 && x0 < p + n) {
+          ctl.b0 = b;
+          ctl.pb0 = p;
+          ctl.found = 1;
+        }
+      }
+      running += chunk_total;
+      __syncthreads();
+      if (ctl.found) break;
+    }
+  }
+  __syncthreads();
+  // no tiles (all barriers idle; nothing in flight); a start that cannot be located means
+  // context_lens changed under the kernel: flag it and do nothing
+  if (x0 >= x1) return;
+  if (!ctl.found) {
+    if (tid == 0) set_dev_err(a.dev_err, PA_DEV_ERR_CONTEXT);
+    return;
+  }
+
+  const int64_t n_tiles = x1 - x0;
+  volatile int* abort_flag = &ctl.abort;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ producer
+    // one bulk copy per token row of the slab (HS*D elements, contiguous in the cache) into
+    // its padded row; the new token's row comes from k_new/v_new on the fused path
+    const uint64_t policy = policy_evict_first();
+    const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
+    const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
+    const int64_t row_elems = (int64_t)Hk * D;
+    const int64_t slab_off = (int64_t)slab * HS * D;
+    int b = ctl.b0;
+    int64_t pb = ctl.pb0;
+    int ctx_b = load_ctx(a.context_lens, b, cap);
+    int nb = (ctx_b + T - 1) / T;
+    constexpr int ROWS_PER_LANE = (2 * T + 31) / 32;
+    for (int64_t it = 0; it < n_tiles; ++it) {
+      const int64_t x = x0 + it;
+      while (x >= pb + nb && b + 1 < B) {
+        pb += nb;
+        ++b;
+        ctx_b = load_ctx(a.context_lens, b, cap);
+        nb = (ctx_b + T - 1) / T;
+      }
+      const int s = (int)(it % kTcStages);
+      const int lt = (int)(x - pb);
+      const int tok0 = lt * T;
+      const int count = min(T, ctx_b - tok0);
+      int flags = 0;
+      if (x == x0 || lt == 0) flags |= kFlagFirst;
+      if (x == x1 - 1 || lt == nb - 1) flags |= kFlagLast;
+      if (pb >= x0 && pb + nb <= x1) flags |= kFlagWhole;
+      int new_row = -1;
+      int64_t new_slot = -1;
+      if (FUSED && lt == nb - 1 && count > 0) {
+        const int pos = ctx_b - 1;
+        const int32_t sl = __ldg(a.slot_mapping + b);
+        if (sl != -1) {
+          const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos / a.block_size);
+          const int64_t want = (blk >= 0 && (int64_t)blk < a.num_blocks)
+                                   ? (int64_t)blk * a.block_size + pos % a.block_size
+                                   : -2;
+          if ((int64_t)sl == want) {
+            new_row = count - 1;
+            new_slot = want;
+          } else if (lane == 0 && slab == 0) {
+            set_dev_err(a.dev_err, PA_DEV_ERR_SLOT);
+          }
+        }
+      }
+      const uint16_t* src[ROWS_PER_LANE];
+      int ok_rows = 0;
+#pragma unroll
+      for (int k = 0; k < ROWS_PER_LANE; ++k) {
+        src[k] = nullptr;
+        const int r = lane + 32 * k;
+        if (r < 2 * T) {
+          const int kv = r >= T;
+          const int t = kv ? r - T : r;
+          if (FUSED && t == new_row) {
+            src[k] = (kv ? static_cast<const uint16_t*>(a.v_new) + (int64_t)b * a.v_new_stride
+                         : static_cast<const uint16_t*>(a.k_new) + (int64_t)b * a.k_new_stride) +
+                     slab_off;
+            ++ok_rows;
+          } else if (t < count) {
+            const int pos = tok0 + t;
+            const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos / a.block_size);
+            if (blk >= 0 && (int64_t)blk < a.num_blocks) {
+              const int64_t rowi = (int64_t)blk * a.block_size + pos % a.block_size;
+              src[k] = (kv ? vc : kc) + rowi * row_elems + slab_off;
+              ++ok_rows;
+            } else if (kv == 0) {
+              set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
+            }
+          }
+        }
+      }
+      const int total_rows = __reduce_add_sync(0xffffffffu, ok_rows);
+      const bool first = flags & kFlagFirst;
+      const uint32_t q_bytes = (uint32_t)(HS * G * D * 2);
+      const uint32_t bytes = (uint32_t)total_rows * TC::ROW + (first ? q_bytes : 0);
+      if (it >= kTcStages) {
+        if (!mbar_wait(&ctl.empty[s], (uint32_t)(((it / kTcStages) - 1) & 1), abort_flag)) {
+          if (lane == 0) {
+            ctl.abort = 1;
+            set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+          }
+        }
+      }
+      unsigned char* st = smem + (size_t)s * TC::STAGE_BYTES;
+      if (lane == 0) {
+        StageMeta& m = ctl.meta[s];
+        m.pb = pb;
+        m.b = b;
+        m.tok0 = tok0;
+        m.count = count;
+        m.nb = nb;
+        m.flags = flags;
+        m.new_row = new_row;
+        m.new_slot = new_slot;
+        mbar_arrive_expect_tx(&ctl.full[s], bytes);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < ROWS_PER_LANE; ++k) {
+        const int r = lane + 32 * k;
+        if (src[k] != nullptr) {
+          const int kv = r >= T;
+          const int t = kv ? r - T : r;
+          bulk_g2s_hint(st + kv * TC::KV_BYTES + t * TC::RS, src[k], TC::ROW, &ctl.full[s], policy);
+        }
+      }
+      if (first && lane == 0) {
+        const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) +
+                               ((int64_t)b * H + (int64_t)slab * HS * G) * D;
+        bulk_g2s(st + 2 * TC::KV_BYTES, qsrc, q_bytes, &ctl.full[s]);
+      }
+    }
+    const int64_t first_drain = n_tiles > kTcStages ? n_tiles - kTcStages : 0;
+    for (int64_t it = first_drain; it < n_tiles; ++it) {
+      const int s = (int)(it % kTcStages);
+      mbar_wait(&ctl.full[s], (uint32_t)((it / kTcStages) & 1), abort_flag);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumers
+  const int j = warp / TC::WPH;   // KV head within the slab
+  const int w = warp % TC::WPH;   // token group within the tile
+  const int kvh = slab * HS + j;  // global KV head
+  // mma fragment coordinates: this thread holds row gid (a query head of the group; rows
+  // 8..15 of the 16-row tile are padding) and columns 2tig, 2tig+1 of each 8-column tile
+  const int gid = lane >> 2, tig = lane & 3;
+  const bool row_ok = gid < G;
+  constexpr int KC = D / 16;      // 16-dim chunks
+  constexpr int NO = D / 8;       // 8-dim output column tiles
+  uint32_t qa[KC][2];             // Q fragments of row gid: dims 16kc + 2tig(+1), +8
+  float o[NO][2];                 // O accumulators of row gid: dims 8n + 2tig, +1
+  float2 z = make_float2(0.f, 0.f);  // accumulators of the padding rows (never read)
+  float m_run = -INFINITY, l_part = 0.f;  // row gid: running max (log2 units), partial sum
+#pragma unroll
+  for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = 0.f;
+  const float sl2 = a.scale_log2;
+
+  int seg_count = 0;
+  for (int64_t it = 0; it < n_tiles; ++it) {
+    const int s = (int)(it % kTcStages);
+    if (!mbar_wait(&ctl.full[s], (uint32_t)((it / kTcStages) & 1), abort_flag)) {
+      if (lane == 0) {
+        ctl.abort = 1;
+        set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+      }
+    }
+    const StageMeta meta = ctl.meta[s];
+    unsigned char* Kst = smem + (size_t)s * TC::STAGE_BYTES;
+    unsigned char* Vst = Kst + TC::KV_BYTES;
+    const int count = meta.count;
+    const int tw0 = w * 16;  // this warp's first token of the tile
+
+    if (meta.flags & kFlagFirst) {
+      const unsigned char* Qst = Kst + 2 * TC::KV_BYTES;
+#pragma unroll
+      for (int kc = 0; kc < KC; ++kc) {
+        const unsigned char* r0 = Qst + ((j * G + gid) * D + kc * 16 + 2 * tig) * 2;
+        qa[kc][0] = row_ok ? *reinterpret_cast<const uint32_t*>(r0) : 0u;
+        qa[kc][1] = row_ok ? *reinterpret_cast<const uint32_t*>(r0 + 16) : 0u;
+      }
+#pragma unroll
+      for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = 0.f;
+      m_run = -INFINITY;
+      l_part = 0.f;
+    }
+
+    // rows of this warp's V past the tile's valid tokens: zero them (head j's columns)
+    if (tw0 + 16 > count) {
+      for (int i = lane; i < 16 * (D / 8); i += 32) {
+        const int t = tw0 + i / (D / 8);
+        if (t >= count)
+          *reinterpret_cast<uint4*>(Vst + (size_t)t * TC::RS + j * D * 2 + (i % (D / 8)) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    if constexpr (FUSED) {
+      // the new token's row of KV head kvh: copied from shared memory to its cache slot
+      if (meta.new_row >= tw0 && meta.new_row < tw0 + 16) {
+        const int64_t dst = meta.new_slot * ((int64_t)Hk * D) + (int64_t)kvh * D;
+        const int half = lane >> 4, sub = lane & 15;
+        if (sub < D / 8) {
+          const unsigned char* srcp = (half ? Vst : Kst) + (size_t)meta.new_row * TC::RS + j * D * 2 + sub * 16;
+          uint16_t* cache = static_cast<uint16_t*>(const_cast<void*>(half ? a.v_cache : a.k_cache));
+          *reinterpret_cast<uint4*>(cache + dst + sub * 8) = *reinterpret_cast<const uint4*>(srcp);
+        }
+      }
+    }
+
+    // ---- S = Q K^T for 16 tokens: two 8-token column tiles ----------------------------
+    float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // row gid, tokens 8n + 2tig, +1
+    {
+      const int tok = tw0 + (lane & 7) + ((lane >> 4) << 3);
+      const unsigned char* kb = Kst + (size_t)tok * TC::RS + j * D * 2 + ((lane >> 3) & 1) * 16;
+#pragma unroll
+      for (int kc = 0; kc < KC; ++kc) {
+        uint32_t r[4];
+        ldsm_x4(r, kb + kc * 32);
+        mma16816<F16>(sc[0][0], sc[0][1], z, qa[kc][0], qa[kc][1], r[0], r[1]);
+        mma16816<F16>(sc[1][0], sc[1][1], z, qa[kc][0], qa[kc][1], r[2], r[3]);
+      }
+    }
+    // ---- online softmax in the accumulator layout (a row's scores sit in one quad) -----
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = tw0 + n * 8 + 2 * tig + e;
+        const float v = t < count ? sc[n][e] * sl2 : -INFINITY;
+        sc[n][e] = v;
+        tmax = fmaxf(tmax, v);
+      }
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+    const float m_new = fmaxf(m_run, tmax);
+    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
+    m_run = m_new;
+    float p[2][2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) p[n][e] = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[n][e] - m_new);
+    l_part = l_part * alpha + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < NO; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
+      }
+    }
+    // ---- O += P V: P (row gid x 16 tokens) straight from the S accumulators ------------
+    const uint32_t pa0 = f2_elt2<F16>(p[0][0], p[0][1]);  // tokens 2tig, +1
+    const uint32_t pa2 = f2_elt2<F16>(p[1][0], p[1][1]);  // tokens 8 + 2tig, +1
+    {
+      const int tok = tw0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const unsigned char* vb = Vst + (size_t)tok * TC::RS + j * D * 2 + (lane >> 4) * 16;
+#pragma unroll
+      for (int dn = 0; dn < D / 16; ++dn) {
+        uint32_t r[4];
+        ldsm_x4_t(r, vb + dn * 32);
+        mma16816<F16>(o[2 * dn][0], o[2 * dn][1], z, pa0, pa2, r[0], r[1]);
+        mma16816<F16>(o[2 * dn + 1][0], o[2 * dn + 1][1], z, pa0, pa2, r[2], r[3]);
+      }
+    }
+
+    if (meta.flags & kFlagLast) {
+      // ---- finalize the segment ----------------------------------------------------
+      float l_all = l_part;
+      l_all += __shfl_xor_sync(0xffffffffu, l_all, 1);
+      l_all += __shfl_xor_sync(0xffffffffu, l_all, 2);
+      // several warps per KV head: merge their softmax states through the stage's K/V
+      // shared memory once every consumer warp is done with it
+      if constexpr (TC::WPH > 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.seg_bar);
+        if (!mbar_wait(&ctl.seg_bar, (uint32_t)(seg_count & 1), abort_flag)) {
+          if (lane == 0) {
+            ctl.abort = 1;
+            set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+          }
+        }
+      }
+      float* merge = reinterpret_cast<float*>(smem + (size_t)s * TC::STAGE_BYTES) +
+                     (size_t)j * (TC::WPH - 1) * TC::MERGE_FLOATS;
+      if (w != 0) {
+        float* mine = merge + (size_t)(w - 1) * TC::MERGE_FLOATS;
+        if (row_ok) {
+#pragma unroll
+          for (int n = 0; n < NO; ++n)
+            *reinterpret_cast<float2*>(mine + gid * D + n * 8 + 2 * tig) = make_float2(o[n][0], o[n][1]);
+          if (tig == 0) {
+            mine[kTcGMax * D + gid] = m_run;
+            mine[kTcGMax * D + kTcGMax + gid] = l_all;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.merge_bar[j]);
+      } else {
+        if constexpr (TC::WPH > 1) {
+          if (!mbar_wait(&ctl.merge_bar[j], (uint32_t)(seg_count & 1), abort_flag)) {
+            if (lane == 0) {
+              ctl.abort = 1;
+              set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+            }
+          }
+        }
+        for (int w2 = 1; w2 < TC::WPH; ++w2) {
+          const float* other = merge + (size_t)(w2 - 1) * TC::MERGE_FLOATS;
+          if (row_ok) {
+            const float m2 = other[kTcGMax * D + gid];
+            const float l2 = other[kTcGMax * D + kTcGMax + gid];
+            const float mm = fmaxf(m_run, m2);
+            const float a1 = (mm == -INFINITY) ? 0.f : fast_exp2(m_run - mm);
+            const float a2 = (mm == -INFINITY) ? 0.f : fast_exp2(m2 - mm);
+#pragma unroll
+            for (int n = 0; n < NO; ++n) {
+              const float2 ov = *reinterpret_cast<const float2*>(other + gid * D + n * 8 + 2 * tig);
+              o[n][0] = o[n][0] * a1 + ov.x * a2;
+              o[n][1] = o[n][1] * a1 + ov.y * a2;
+            }
+            l_all = l_all * a1 + l2 * a2;
+            m_run = mm;
+          }
+        }
+        // normalise and write the rows, or the partials for the combine
+        const int b = meta.b;
+        if (meta.flags & kFlagWhole) {
+          if (row_ok) {
+            const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
+            uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)b * H + kvh * G + gid) * D;
+#pragma unroll
+            for (int n = 0; n < NO; ++n)
+              *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * tig) =
+                  f2_elt2<F16>(o[n][0] * inv, o[n][1] * inv);
+          }
+        } else {
+          const int slot = (x0 < meta.pb) ? 1 : 0;
+          if (row_ok) {
+            const int hg = kvh * G + gid;
+            const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
+            float* dst = a.part_o + (((int64_t)c * 2 + slot) * H + hg) * D;
+#pragma unroll
+            for (int n = 0; n < NO; ++n)
+              *reinterpret_cast<float2*>(dst + n * 8 + 2 * tig) = make_float2(o[n][0] * inv, o[n][1] * inv);
+            if (tig == 0)
+              a.part_lse[((int64_t)c * 2 + slot) * H + hg] =
+                  (l_all > 0.f) ? m_run + fast_log2(l_all) : -INFINITY;
+          }
+          __threadfence();
+          __syncwarp();
+          int old = 0;
+          int* counter = a.counters + (int64_t)b * Hk + kvh;
+          if (lane == 0) old = atomicAdd(counter, 1);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          const int64_t c_lo = cta_of(meta.pb, NT, g_eff);
+          const int64_t c_hi = cta_of(meta.pb + meta.nb - 1, NT, g_eff);
+          const int nseg = (int)(c_hi - c_lo + 1);
+          if (old == nseg - 1) {
+            // (4) last arrival: combine the partials of sequence b in CTA order
+            __threadfence();
+#pragma unroll 1
+            for (int hh = 0; hh < G; ++hh) {
+              const int hg = kvh * G + hh;
+              float mx = -INFINITY;
+              for (int k0 = 0; k0 < nseg; k0 += 32) {
+                const int64_t c2 = c_lo + k0 + lane;
+                if (k0 + lane < nseg) {
+                  const int sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
+                  mx = fmaxf(mx, __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg));
+                }
+              }
+#pragma unroll
+              for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+              constexpr int CPL = D / 32;  // combined dims per lane
+              float acc[CPL];
+#pragma unroll
+              for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
+              float den = 0.f;
+              for (int k0 = 0; k0 < nseg; k0 += 32) {
+                const int64_t c2 = c_lo + k0 + lane;
+                float wgt = 0.f;
+                int sl = 0;
+                if (k0 + lane < nseg) {
+                  sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
+                  const float ls = __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg);
+                  wgt = (mx == -INFINITY || ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
+                }
+                const int nk = min(32, nseg - k0);
+                for (int k = 0; k < nk; ++k) {
+                  const float wk = __shfl_sync(0xffffffffu, wgt, k);
+                  const int slk = __shfl_sync(0xffffffffu, sl, k);
+                  const int64_t ck = c_lo + k0 + k;
+                  den += wk;
+                  if (wk != 0.f) {
+                    const float* src = a.part_o + ((ck * 2 + slk) * H + hg) * D + lane * CPL;
+                    if constexpr (CPL == 4) {
+                      const float4 po = __ldcg(reinterpret_cast<const float4*>(src));
+                      acc[0] = fmaf(wk, po.x, acc[0]);
+                      acc[1] = fmaf(wk, po.y, acc[1]);
+                      acc[2] = fmaf(wk, po.z, acc[2]);
+                      acc[3] = fmaf(wk, po.w, acc[3]);
+                    } else {
+                      const float2 po = __ldcg(reinterpret_cast<const float2*>(src));
+                      acc[0] = fmaf(wk, po.x, acc[0]);
+                      acc[1] = fmaf(wk, po.y, acc[1]);
+                    }
+                  }
+                }
+              }
+              const float inv = den > 0.f ? 1.f / den : 0.f;
+              uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)b * H + hg) * D + lane * CPL;
+              if constexpr (CPL == 4) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(f2_elt2<F16>(acc[0] * inv, acc[1] * inv),
+                                                            f2_elt2<F16>(acc[2] * inv, acc[3] * inv));
+              } else {
+                *reinterpret_cast<uint32_t*>(dst) = f2_elt2<F16>(acc[0] * inv, acc[1] * inv);
+              }
+            }
+            if (lane == 0) *counter = 0;  // leave the counter zero for the next call
+          }
+        }
+      }
+      ++seg_count;
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.empty[s]);
+  }
+}
+
+template <int HS, bool FUSED, int D, bool F16>
+int launch_decode_tc_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
+  using TC = TcCfg<HS, D>;
+  static bool attr_done[64] = {false};
+  const int dev = info.device;
+  if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(paged_decode_tc_kernel<HS, FUSED, D, F16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC::SMEM) != cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  const int slabs = a.num_kv_heads / HS;
+  dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);
+  paged_decode_tc_kernel<HS, FUSED, D, F16><<<grid, kThreads, TC::SMEM, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Every head slab of the tensor-core path for one (FUSED, D, element type) combination.
+template <bool FUSED, int D, bool F16>
+int dispatch_slab_tc(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
+  switch (decode_head_slab(a.num_kv_heads)) {
+    case 8: return launch_decode_tc_t<8, FUSED, D, F16>(a, info, stream);
+    case 4: return launch_decode_tc_t<4, FUSED, D, F16>(a, info, stream);
+    case 2: return launch_decode_tc_t<2, FUSED, D, F16>(a, info, stream);
+    default: return launch_decode_tc_t<1, FUSED, D, F16>(a, info, stream);
+  }
+}
+
+}  // namespace
+}  // namespace pa

@@ -94,6 +94,14 @@ int launch_decode_d128_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStre
 int launch_decode_step_d64_bf16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
 int launch_decode_step_d64_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
 int launch_decode_step_d128_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+// Query-head groups of 3 to 8 per KV head: the tensor-core path (decode_tc.cuh).
+int launch_decode_tc(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+int launch_decode_step_tc(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+// Groups that take the tensor-core path.
+inline bool decode_uses_tc(int num_heads, int num_kv_heads) {
+  const int g = num_heads / num_kv_heads;
+  return g >= 3 && g <= 8;
+}
 // The same kernel with the store of token b (k_new/v_new row b) at slot_mapping[b] fused in;
 // the caches are written, so a.k_cache / a.v_cache must point to writable memory.
 int launch_decode_step(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);

@@ -114,3 +114,31 @@ def test_fp16_large_values_round_as_fp16():
     ref = oracle.decode(case.q, kt, vt, case.block_tables, case.context_lens)
     got = to_f64(out)
     assert np.all(np.abs(got - ref) <= 2 * np.abs(ref) * 2.0 ** -11 + 4096 * 1e-3)
+
+
+@pytest.mark.parametrize("D,dt", [(128, torch.bfloat16)] + VARIANTS, ids=["d128-bf16"] + IDS)
+@pytest.mark.parametrize("H,Hk", [(24, 8), (40, 8), (48, 8), (56, 8), (64, 8), (32, 8), (20, 4),
+                                  (10, 2), (7, 1)])
+def test_tensor_core_groups(D, dt, H, Hk):
+    """Query-head groups of 3..8 per KV head (the tensor-core path; 5 is the 40/8 layout of
+    the 14B-class models): decode and the fused step, long and short contexts, split
+    across CTAs (grid 5) and whole."""
+    case = workloads.decode_case([1, 17, 300, 1500, 0, 64], H, Hk, D, 64,
+                                 seed=2500 + H + 3 * Hk + D, dtype=dt)
+    ok, ov, kt, vt = stored(case)
+    ref = oracle.decode(case.q, kt, vt, case.block_tables, case.context_lens)
+    for grid in (0, 5):
+        dc = DeviceCase(case)
+        dc.store()
+        out = dc.decode(grid_ctas=grid)
+        assert dc.dev_err() == 0
+        got = to_f64(out)
+        assert np.all(np.isfinite(got))
+        assert_close(got, ref, f"decode G={H // Hk} D={D} {dt} grid={grid}")
+        one = DeviceCase(case)
+        o2 = torch.full_like(one.q, float("nan"))
+        pk.pa_decode_step(o2, one.q, one.k_new, one.v_new, one.k_cache, one.v_cache, one.slots,
+                          one.bt, one.ctx, grid_ctas=grid, dev_err=one.err)
+        assert one.dev_err() == 0
+        assert torch.equal(o2.view(torch.int16), out.view(torch.int16))
+        assert torch.equal(one.k_cache.view(torch.int16), dc.k_cache.view(torch.int16))
