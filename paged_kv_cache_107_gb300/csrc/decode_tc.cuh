@@ -9,35 +9,74 @@
 // once G >= 4 (and G = 8 no longer fits in registers); here one warp runs them as
 // 16-row tensor-core products, the G heads padded to 16 rows.
 //
-//  * Token rows of the slab land in shared memory at a stride of row + 16 bytes (one bulk
-//    copy per token row), so the 8 rows an ldmatrix reads sit in 8 different bank groups.
+//  * A stage holds T = 128 / HS tokens of the slab's HS KV heads, K then V, each as D/64
+//    halves laid out [head][token][64 dims]: 128-byte rows with the 128-byte swizzle, so
+//    the 8 token rows an ldmatrix reads sit in 8 different bank groups. The producer fills
+//    it with TMA boxes of tb tokens x HS heads x 64 dims (tb = the largest power of two
+//    dividing block_size, at most T), i.e. 2 * D/64 * T/tb copies per stage; a block size
+//    with no such tb >= 8 is filled with 16-byte cp.async copies into the same layout.
+//  * The fused step's new token: its K and V rows of the slab come from k_new / v_new into
+//    a side row of the stage; lanes whose token is the new one point ldmatrix there.
+//  * Q of a segment goes to its own slot (two where shared memory allows), loaded once per
+//    sequence and released as soon as every warp holds its fragments.
 //  * Warp (j, w): KV head j of the slab, tokens 16w..16w+15 of each tile. S: for every
-//    16-dim chunk, ldmatrix.x4 gives the K fragments of two 8-token column tiles; Q
-//    fragments are loaded once per sequence. Online softmax in the accumulator layout (a
-//    row's 16 scores sit in one quad of lanes); the S accumulators become the A operand of
-//    O += P V directly; V fragments come from ldmatrix.x4.trans. Rows of V past the context
-//    are zeroed first, so no stale value meets a zero probability.
+//    16-dim chunk, ldmatrix.x4 gives the K fragments of two 8-token column tiles. Online
+//    softmax in the accumulator layout (a row's 16 scores sit in one quad of lanes); the S
+//    accumulators become the A operand of O += P V directly; V fragments come from
+//    ldmatrix.x4.trans. Rows of V past the context are zeroed first, so no stale value
+//    meets a zero probability.
 #pragma once
 
+#include <cuda.h>
+#include <string.h>
+
 #include "decode_kernel.cuh"
+#include "tensor_map.h"
 
 namespace pa {
 namespace {
 
 constexpr int kTcGMax = 8;   // query heads per KV head on this path (rows of the 16-row tile)
-constexpr int kTcStages = 2;
+
+template <int S>
+struct TcCtrl {
+  uint64_t full[S];
+  uint64_t empty[S];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t seg_bar;
+  uint64_t merge_bar[8];
+  StageMeta meta[S];
+  int64_t nt;      // tiles in the stream
+  int64_t x0, x1;  // this CTA's tile range
+  int64_t pb0;     // first tile of the sequence holding x0
+  int b0;
+  int g_eff;       // CTAs that own tiles
+  int found;
+  int abort;
+  int64_t red[32];
+};
 
 template <int HS, int D>
 struct TcCfg {
   static constexpr int T = 128 / HS;               // tokens per stage (8 warps x 16 / HS)
   static constexpr int WPH = kConsumerWarps / HS;  // warps per KV head (token split)
-  static constexpr int ROW = HS * D * 2;           // bytes of one token row of the slab
-  static constexpr int RS = ROW + 16;              // its stride in shared memory
-  static constexpr int KV_BYTES = T * RS;
+  static constexpr int NH = D / 64;                // 64-dim halves of a head row
+  static constexpr int HALF = HS * T * 128;        // bytes of one half: [head][token][64 dims]
+  static constexpr int KV_BYTES = NH * HALF;
+  static constexpr int SIDE_ROW = HS * D * 2;      // the new token's K (or V) row of the slab
+  static constexpr int STAGE_BYTES = (2 * KV_BYTES + 2 * SIDE_ROW + 1023) / 1024 * 1024;
   static constexpr int Q_BYTES = HS * kTcGMax * D * 2;
-  static constexpr int STAGE_BYTES = ((2 * KV_BYTES + Q_BYTES) + 127) / 128 * 128;
+  static constexpr int CTRL_BYTES = 1024;
+  static constexpr int BUDGET = 227 * 1024 - 1024 - CTRL_BYTES;  // less the alignment slack
+  static constexpr int QS = (3 * STAGE_BYTES + 2 * Q_BYTES <= BUDGET) ? 2 : 1;
+  static constexpr int FIT = (BUDGET - QS * Q_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = FIT < 6 ? FIT : 6;
   static constexpr int MERGE_FLOATS = kTcGMax * (D + 2);
-  static constexpr size_t SMEM = (size_t)kTcStages * STAGE_BYTES + 4096 + 128;
+  static constexpr size_t SMEM =
+      1024 + (size_t)STAGES * STAGE_BYTES + (size_t)QS * Q_BYTES + CTRL_BYTES;
+  static_assert(STAGES >= 2, "at least two stages");
+  static_assert(sizeof(TcCtrl<STAGES>) <= CTRL_BYTES, "control block");
   static_assert(HS * (WPH - 1) * MERGE_FLOATS * 4 <= 2 * KV_BYTES, "merge scratch");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -63,24 +102,53 @@ __device__ __forceinline__ void mma16816(float& c0, float& c1, float2& z, uint32
         : "r"(a0), "r"(zero), "r"(a2), "r"(zero), "r"(b0), "r"(b1));
   }
 }
-__device__ __forceinline__ void ldsm_x4(uint32_t* r, const void* p) {
+// ldmatrix x4 (plain and transposed) from a 32-bit shared-memory address
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+               : "r"(addr));
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, const void* p) {
+__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
+               : "r"(addr));
+}
+// One TMA box (4-D tensor map) into shared memory, completion counted on `bar` in bytes,
+// with an L2 eviction-priority hint.
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map, int c0, int c1,
+                                                 int c2, int c3, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+// The barrier counts one more arrival, made when this thread's cp.async copies so far land.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 template <int HS, bool FUSED, int D, bool F16>
-__global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
+                           const int tb) {
   using TC = TcCfg<HS, D>;
+  constexpr int S = TC::STAGES;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem + (size_t)kTcStages * TC::STAGE_BYTES);
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* qbuf = smem + (size_t)S * TC::STAGE_BYTES;
+  TcCtrl<S>& ctl = *reinterpret_cast<TcCtrl<S>*>(qbuf + (size_t)TC::QS * TC::Q_BYTES);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -95,9 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
   constexpr int T = TC::T;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&ctl.full[s], 1);
       mbar_init(&ctl.empty[s], kConsumerWarps);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&ctl.q_full[q], 1);
+      mbar_init(&ctl.q_empty[q], kConsumerWarps);
     }
     mbar_init(&ctl.seg_bar, kConsumerWarps);
     if (TC::WPH > 1)
@@ -108,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
     ctl.pb0 = 0;
     fence_mbar_init();
   }
-
   // ---- prologue: total tiles, then the sequence that holds this CTA's first tile -----
   int64_t local = 0;
   for (int b = tid; b < B; b += kThreads) {
@@ -204,18 +275,22 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
-    // one bulk copy per token row of the slab (HS*D elements, contiguous in the cache) into
-    // its padded row; the new token's row comes from k_new/v_new on the fused path
     const uint64_t policy = policy_evict_first();
+    if (tb > 0 && lane == 0) {
+      prefetch_tensor_map(&tm_k);
+      prefetch_tensor_map(&tm_v);
+    }
     const uint16_t* kc = static_cast<const uint16_t*>(a.k_cache);
     const uint16_t* vc = static_cast<const uint16_t*>(a.v_cache);
     const int64_t row_elems = (int64_t)Hk * D;
     const int64_t slab_off = (int64_t)slab * HS * D;
+    const int box_bytes = HS * tb * 128;  // one box: HS heads x tb tokens x 64 dims
+    const int nbx = tb > 0 ? T / tb : 0;  // boxes per half
     int b = ctl.b0;
     int64_t pb = ctl.pb0;
     int ctx_b = load_ctx(a.context_lens, b, cap);
     int nb = (ctx_b + T - 1) / T;
-    constexpr int ROWS_PER_LANE = (2 * T + 31) / 32;
+    int q_n = 0;  // segments whose Q has been issued
     for (int64_t it = 0; it < n_tiles; ++it) {
       const int64_t x = x0 + it;
       while (x >= pb + nb && b + 1 < B) {
@@ -224,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
         ctx_b = load_ctx(a.context_lens, b, cap);
         nb = (ctx_b + T - 1) / T;
       }
-      const int s = (int)(it % kTcStages);
+      const int s = (int)(it % S);
       const int lt = (int)(x - pb);
       const int tok0 = lt * T;
       const int count = min(T, ctx_b - tok0);
@@ -250,39 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
           }
         }
       }
-      const uint16_t* src[ROWS_PER_LANE];
-      int ok_rows = 0;
-#pragma unroll
-      for (int k = 0; k < ROWS_PER_LANE; ++k) {
-        src[k] = nullptr;
-        const int r = lane + 32 * k;
-        if (r < 2 * T) {
-          const int kv = r >= T;
-          const int t = kv ? r - T : r;
-          if (FUSED && t == new_row) {
-            src[k] = (kv ? static_cast<const uint16_t*>(a.v_new) + (int64_t)b * a.v_new_stride
-                         : static_cast<const uint16_t*>(a.k_new) + (int64_t)b * a.k_new_stride) +
-                     slab_off;
-            ++ok_rows;
-          } else if (t < count) {
-            const int pos = tok0 + t;
-            const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos / a.block_size);
-            if (blk >= 0 && (int64_t)blk < a.num_blocks) {
-              const int64_t rowi = (int64_t)blk * a.block_size + pos % a.block_size;
-              src[k] = (kv ? vc : kc) + rowi * row_elems + slab_off;
-              ++ok_rows;
-            } else if (kv == 0) {
-              set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
-            }
-          }
-        }
+      // this lane's box: tokens tok0 + lane*tb .. +tb-1, inside one block
+      int blk = -1, off = 0;
+      bool box_ok = false;
+      if (lane < nbx && lane * tb < count) {
+        const int pos = tok0 + lane * tb;
+        blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos / a.block_size);
+        off = pos % a.block_size;
+        box_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+        if (!box_ok) set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
       }
-      const int total_rows = __reduce_add_sync(0xffffffffu, ok_rows);
-      const bool first = flags & kFlagFirst;
-      const uint32_t q_bytes = (uint32_t)(HS * G * D * 2);
-      const uint32_t bytes = (uint32_t)total_rows * TC::ROW + (first ? q_bytes : 0);
-      if (it >= kTcStages) {
-        if (!mbar_wait(&ctl.empty[s], (uint32_t)(((it / kTcStages) - 1) & 1), abort_flag)) {
+      const int nbox = __popc(__ballot_sync(0xffffffffu, box_ok));
+      if (it >= S) {
+        if (!mbar_wait(&ctl.empty[s], (uint32_t)(((it / S) - 1) & 1), abort_flag)) {
           if (lane == 0) {
             ctl.abort = 1;
             set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
@@ -290,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
         }
       }
       unsigned char* st = smem + (size_t)s * TC::STAGE_BYTES;
+      unsigned char* side = st + 2 * TC::KV_BYTES;
       if (lane == 0) {
         StageMeta& m = ctl.meta[s];
         m.pb = pb;
@@ -300,29 +356,91 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
         m.flags = flags;
         m.new_row = new_row;
         m.new_slot = new_slot;
-        mbar_arrive_expect_tx(&ctl.full[s], bytes);
+        if (tb > 0)
+          mbar_arrive_expect_tx(&ctl.full[s], (uint32_t)(nbox * 2 * TC::NH * box_bytes +
+                                                         (new_row >= 0 ? 2 * TC::SIDE_ROW : 0)));
       }
       __syncwarp();
+      if (tb > 0) {
+        if (box_ok) {
 #pragma unroll
-      for (int k = 0; k < ROWS_PER_LANE; ++k) {
-        const int r = lane + 32 * k;
-        if (src[k] != nullptr) {
-          const int kv = r >= T;
-          const int t = kv ? r - T : r;
-          bulk_g2s_hint(st + kv * TC::KV_BYTES + t * TC::RS, src[k], TC::ROW, &ctl.full[s], policy);
+          for (int h = 0; h < TC::NH; ++h) {
+            tma_load_4d_hint(st + h * TC::HALF + lane * box_bytes, &tm_k, h * 64, off, slab * HS,
+                             blk, &ctl.full[s], policy);
+            tma_load_4d_hint(st + TC::KV_BYTES + h * TC::HALF + lane * box_bytes, &tm_v, h * 64,
+                             off, slab * HS, blk, &ctl.full[s], policy);
+          }
         }
+        if (FUSED && new_row >= 0 && lane == 0) {
+          bulk_g2s(side, static_cast<const uint16_t*>(a.k_new) + (int64_t)b * a.k_new_stride + slab_off,
+                   TC::SIDE_ROW, &ctl.full[s]);
+          bulk_g2s(side + TC::SIDE_ROW,
+                   static_cast<const uint16_t*>(a.v_new) + (int64_t)b * a.v_new_stride + slab_off,
+                   TC::SIDE_ROW, &ctl.full[s]);
+        }
+      } else {
+        // 16-byte copies into the same swizzled layout, one box of T tokens per half
+        constexpr int CH = D / 8;  // 16-byte chunks of one head's row
+        const int per_kv = count * HS * CH;
+        for (int i = lane; i < 2 * per_kv; i += 32) {
+          const int kv = i >= per_kv;
+          const int r = kv ? i - per_kv : i;
+          const int t = r / (HS * CH);
+          const int jj = (r / CH) % HS;
+          const int ch = r % CH;
+          if (FUSED && t == new_row) {
+            const uint16_t* src =
+                (kv ? static_cast<const uint16_t*>(a.v_new) + (int64_t)b * a.v_new_stride
+                    : static_cast<const uint16_t*>(a.k_new) + (int64_t)b * a.k_new_stride) +
+                slab_off + jj * D + ch * 8;
+            cp_async16(side + kv * TC::SIDE_ROW + (jj * D + ch * 8) * 2, src);
+          } else {
+            const int pos = tok0 + t;
+            const int bk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + pos / a.block_size);
+            if (bk < 0 || (int64_t)bk >= a.num_blocks) {
+              if (kv == 0 && jj == 0 && ch == 0) set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
+              continue;
+            }
+            const int64_t rowi = (int64_t)bk * a.block_size + pos % a.block_size;
+            const uint16_t* src = (kv ? vc : kc) + rowi * row_elems + slab_off + jj * D + ch * 8;
+            cp_async16(st + kv * TC::KV_BYTES + (ch >> 3) * TC::HALF + (jj * T + t) * 128 +
+                           (((ch & 7) ^ (t & 7)) << 4),
+                       src);
+          }
+        }
+        cp_async_arrive(&ctl.full[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.full[s]);
       }
-      if (first && lane == 0) {
-        const uint16_t* qsrc = static_cast<const uint16_t*>(a.q) +
-                               ((int64_t)b * H + (int64_t)slab * HS * G) * D;
-        bulk_g2s(st + 2 * TC::KV_BYTES, qsrc, q_bytes, &ctl.full[s]);
+      if (flags & kFlagFirst) {
+        // Q of the segment (HS*G rows of D, contiguous) into its slot
+        const int qs = q_n % TC::QS;
+        if (q_n >= TC::QS) {
+          if (!mbar_wait(&ctl.q_empty[qs], (uint32_t)(((q_n / TC::QS) - 1) & 1), abort_flag)) {
+            if (lane == 0) {
+              ctl.abort = 1;
+              set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+            }
+          }
+        }
+        if (lane == 0) {
+          const uint32_t q_bytes = (uint32_t)(HS * G * D * 2);
+          mbar_arrive_expect_tx(&ctl.q_full[qs], q_bytes);
+          bulk_g2s(qbuf + (size_t)qs * TC::Q_BYTES,
+                   static_cast<const uint16_t*>(a.q) + ((int64_t)b * H + (int64_t)slab * HS * G) * D,
+                   q_bytes, &ctl.q_full[qs]);
+        }
+        ++q_n;
       }
     }
-    const int64_t first_drain = n_tiles > kTcStages ? n_tiles - kTcStages : 0;
+    // copies still in flight land before the producer leaves (bounded waits)
+    const int64_t first_drain = n_tiles > S ? n_tiles - S : 0;
     for (int64_t it = first_drain; it < n_tiles; ++it) {
-      const int s = (int)(it % kTcStages);
-      mbar_wait(&ctl.full[s], (uint32_t)((it / kTcStages) & 1), abort_flag);
+      const int s = (int)(it % S);
+      mbar_wait(&ctl.full[s], (uint32_t)((it / S) & 1), abort_flag);
     }
+    for (int n = q_n > TC::QS ? q_n - TC::QS : 0; n < q_n; ++n)
+      mbar_wait(&ctl.q_full[n % TC::QS], (uint32_t)((n / TC::QS) & 1), abort_flag);
     return;
   }
 
@@ -344,10 +462,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
   for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = 0.f;
   const float sl2 = a.scale_log2;
 
+  // shared-memory row of token t of head j within a half: boxes of tbl tokens, each
+  // [head][token]; chunk c of the row sits at chunk c ^ (t % 8)
+  const int tbl = tb > 0 ? tb : T;
+  const int lg_tbl = __ffs(tbl) - 1;
+  const int tw0 = w * 16;  // this warp's first token of the tile
+  auto row_off = [&](int t) -> int {
+    return ((((t >> lg_tbl) * HS + j) << lg_tbl) + (t & (tbl - 1))) * 128;
+  };
+  const int tK = tw0 + (lane & 7) + ((lane >> 4) << 3);        // ldmatrix row (K, S product)
+  const int tV = tw0 + (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row (V, trans)
+  const int sw = lane & 7;                                   // = t % 8 of both rows
+  const int k_hi = (lane >> 3) & 1, v_hi = lane >> 4;        // second 8 dims of a 16-dim chunk
+  // byte offsets within a stage: 16-byte chunk c = 2*(chunk16 % 4) + hi of a 128-byte row sits
+  // at (c ^ sw) * 16 = ((chunk16 % 4) * 32 ^ (sw & 6) * 16) + (hi ^ (sw & 1)) * 16
+  const uint32_t x_sw = (uint32_t)(sw & 6) << 4;
+  const uint32_t k_lane = (uint32_t)row_off(tK) + ((uint32_t)(k_hi ^ (sw & 1)) << 4);
+  const uint32_t v_lane = (uint32_t)(TC::KV_BYTES + row_off(tV)) + ((uint32_t)(v_hi ^ (sw & 1)) << 4);
+  const uint32_t ks_lane = (uint32_t)(2 * TC::KV_BYTES + (j * D + k_hi * 8) * 2);
+  const uint32_t vs_lane = (uint32_t)(2 * TC::KV_BYTES + TC::SIDE_ROW + (j * D + v_hi * 8) * 2);
+  const uint32_t smem_base = smem_u32(smem);
+
   int seg_count = 0;
+  int q_n = 0;
   for (int64_t it = 0; it < n_tiles; ++it) {
-    const int s = (int)(it % kTcStages);
-    if (!mbar_wait(&ctl.full[s], (uint32_t)((it / kTcStages) & 1), abort_flag)) {
+    const int s = (int)(it % S);
+    if (!mbar_wait(&ctl.full[s], (uint32_t)((it / S) & 1), abort_flag)) {
       if (lane == 0) {
         ctl.abort = 1;
         set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
@@ -356,55 +496,70 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
     const StageMeta meta = ctl.meta[s];
     unsigned char* Kst = smem + (size_t)s * TC::STAGE_BYTES;
     unsigned char* Vst = Kst + TC::KV_BYTES;
+    unsigned char* side = Kst + 2 * TC::KV_BYTES;
     const int count = meta.count;
-    const int tw0 = w * 16;  // this warp's first token of the tile
 
     if (meta.flags & kFlagFirst) {
-      const unsigned char* Qst = Kst + 2 * TC::KV_BYTES;
+      const int qs = q_n % TC::QS;
+      if (!mbar_wait(&ctl.q_full[qs], (uint32_t)((q_n / TC::QS) & 1), abort_flag)) {
+        if (lane == 0) {
+          ctl.abort = 1;
+          set_dev_err(a.dev_err, PA_DEV_ERR_TIMEOUT);
+        }
+      }
+      const unsigned char* Qst = qbuf + (size_t)qs * TC::Q_BYTES;
 #pragma unroll
       for (int kc = 0; kc < KC; ++kc) {
         const unsigned char* r0 = Qst + ((j * G + gid) * D + kc * 16 + 2 * tig) * 2;
         qa[kc][0] = row_ok ? *reinterpret_cast<const uint32_t*>(r0) : 0u;
         qa[kc][1] = row_ok ? *reinterpret_cast<const uint32_t*>(r0 + 16) : 0u;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.q_empty[qs]);
+      ++q_n;
 #pragma unroll
       for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = 0.f;
       m_run = -INFINITY;
       l_part = 0.f;
     }
 
-    // rows of this warp's V past the tile's valid tokens: zero them (head j's columns)
+    // rows of this warp's V past the tile's valid tokens: zero them (head j's rows)
     if (tw0 + 16 > count) {
-      for (int i = lane; i < 16 * (D / 8); i += 32) {
-        const int t = tw0 + i / (D / 8);
+      for (int i = lane; i < 16 * TC::NH * 8; i += 32) {
+        const int t = tw0 + i / (TC::NH * 8);
         if (t >= count)
-          *reinterpret_cast<uint4*>(Vst + (size_t)t * TC::RS + j * D * 2 + (i % (D / 8)) * 16) =
+          *reinterpret_cast<uint4*>(Vst + ((i >> 3) % TC::NH) * TC::HALF + row_off(t) + (i & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
       }
+      fence_proxy_async_smem();
       __syncwarp();
     }
+    bool k_new_lane = false, v_new_lane = false;
     if constexpr (FUSED) {
-      // the new token's row of KV head kvh: copied from shared memory to its cache slot
+      // the new token's row of KV head kvh: from the side rows to its cache slot
       if (meta.new_row >= tw0 && meta.new_row < tw0 + 16) {
         const int64_t dst = meta.new_slot * ((int64_t)Hk * D) + (int64_t)kvh * D;
         const int half = lane >> 4, sub = lane & 15;
         if (sub < D / 8) {
-          const unsigned char* srcp = (half ? Vst : Kst) + (size_t)meta.new_row * TC::RS + j * D * 2 + sub * 16;
+          const unsigned char* srcp = side + half * TC::SIDE_ROW + j * D * 2 + sub * 16;
           uint16_t* cache = static_cast<uint16_t*>(const_cast<void*>(half ? a.v_cache : a.k_cache));
           *reinterpret_cast<uint4*>(cache + dst + sub * 8) = *reinterpret_cast<const uint4*>(srcp);
         }
       }
+      k_new_lane = tK == meta.new_row;
+      v_new_lane = tV == meta.new_row;
     }
 
     // ---- S = Q K^T for 16 tokens: two 8-token column tiles ----------------------------
     float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // row gid, tokens 8n + 2tig, +1
+    const uint32_t st_u = smem_base + (uint32_t)s * TC::STAGE_BYTES;
     {
-      const int tok = tw0 + (lane & 7) + ((lane >> 4) << 3);
-      const unsigned char* kb = Kst + (size_t)tok * TC::RS + j * D * 2 + ((lane >> 3) & 1) * 16;
 #pragma unroll
       for (int kc = 0; kc < KC; ++kc) {
         uint32_t r[4];
-        ldsm_x4(r, kb + kc * 32);
+        uint32_t kp = st_u + k_lane + (kc >> 2) * TC::HALF + (((uint32_t)(kc & 3) << 5) ^ x_sw);
+        if constexpr (FUSED) kp = k_new_lane ? st_u + ks_lane + kc * 32 : kp;
+        ldsm_x4(r, kp);
         mma16816<F16>(sc[0][0], sc[0][1], z, qa[kc][0], qa[kc][1], r[0], r[1]);
         mma16816<F16>(sc[1][0], sc[1][1], z, qa[kc][0], qa[kc][1], r[2], r[3]);
       }
@@ -442,12 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
     const uint32_t pa0 = f2_elt2<F16>(p[0][0], p[0][1]);  // tokens 2tig, +1
     const uint32_t pa2 = f2_elt2<F16>(p[1][0], p[1][1]);  // tokens 8 + 2tig, +1
     {
-      const int tok = tw0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-      const unsigned char* vb = Vst + (size_t)tok * TC::RS + j * D * 2 + (lane >> 4) * 16;
 #pragma unroll
       for (int dn = 0; dn < D / 16; ++dn) {
         uint32_t r[4];
-        ldsm_x4_t(r, vb + dn * 32);
+        uint32_t vp = st_u + v_lane + (dn >> 2) * TC::HALF + (((uint32_t)(dn & 3) << 5) ^ x_sw);
+        if constexpr (FUSED) vp = v_new_lane ? st_u + vs_lane + dn * 32 : vp;
+        ldsm_x4_t(r, vp);
         mma16816<F16>(o[2 * dn][0], o[2 * dn][1], z, pa0, pa2, r[0], r[1]);
         mma16816<F16>(o[2 * dn + 1][0], o[2 * dn + 1][1], z, pa0, pa2, r[2], r[3]);
       }
@@ -470,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_decode_tc_kernel(const Deco
           }
         }
       }
-      float* merge = reinterpret_cast<float*>(smem + (size_t)s * TC::STAGE_BYTES) +
+      float* merge = reinterpret_cast<float*>(Kst) +
                      (size_t)j * (TC::WPH - 1) * TC::MERGE_FLOATS;
       if (w != 0) {
         float* mine = merge + (size_t)(w - 1) * TC::MERGE_FLOATS;
@@ -631,9 +786,22 @@ int launch_decode_tc_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t
       return PA_ERR_CUDA;
     attr_done[dev] = true;
   }
+  // tokens per TMA box: the largest power of two dividing block_size, at most a stage's
+  // tokens; below 8 the stage is filled by 16-byte cp.async copies instead
+  int tb = a.block_size & -a.block_size;
+  if (tb > TC::T) tb = TC::T;
+  if (tb < 8) tb = 0;
+  CUtensorMap mk, mv;
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  if (tb > 0 && (!make_slab_map(&mk, a.k_cache, a.num_kv_heads, D, F16, a.block_size,
+                                a.num_blocks, tb, HS) ||
+                 !make_slab_map(&mv, a.v_cache, a.num_kv_heads, D, F16, a.block_size,
+                                a.num_blocks, tb, HS)))
+    return PA_ERR_CUDA;
   const int slabs = a.num_kv_heads / HS;
   dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);
-  paged_decode_tc_kernel<HS, FUSED, D, F16><<<grid, kThreads, TC::SMEM, stream>>>(a);
+  paged_decode_tc_kernel<HS, FUSED, D, F16><<<grid, kThreads, TC::SMEM, stream>>>(mk, mv, a, tb);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

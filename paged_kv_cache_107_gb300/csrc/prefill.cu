@@ -2,28 +2,15 @@
 // the supported shapes, and the launch of the prefill kernel (prefill_kernel.cuh); head_dim
 // 128 with bf16 is instantiated here, the other combinations in prefill_d*_*.cu.
 #include "prefill_kernel.cuh"
+#include "tensor_map.h"
 
 namespace pa {
 namespace {
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int head_dim,
                     bool f16, int block_size, int64_t num_blocks) {
-  auto encode = get_encode();
+  auto encode = tmap_encode_fn();
   if (!encode) return false;
   const int box_rows = block_size < kKeys ? block_size : kKeys;
   cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,

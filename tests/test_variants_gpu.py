@@ -142,3 +142,33 @@ def test_tensor_core_groups(D, dt, H, Hk):
         assert one.dev_err() == 0
         assert torch.equal(o2.view(torch.int16), out.view(torch.int16))
         assert torch.equal(one.k_cache.view(torch.int16), dc.k_cache.view(torch.int16))
+
+
+@pytest.mark.parametrize("bs", [5, 8, 12, 16, 24, 48, 256])
+@pytest.mark.parametrize("H,Hk,D", [(32, 8, 128), (64, 8, 64), (16, 2, 128), (8, 1, 128),
+                                    (12, 4, 64)])
+def test_tensor_core_block_sizes(bs, H, Hk, D):
+    """The tensor-core path's stage fill for every kind of block size: TMA boxes of a whole
+    stage (256), of 8 to 48 tokens (several boxes per stage: 8, 16, 24 -> boxes of 8, 48 ->
+    boxes of 16), and 16-byte copies where no box of 8 or more tokens fits a block (5, 12).
+    Cache tails past each context hold NaN; decode and the fused step, split and whole."""
+    case = workloads.decode_case([1, 9, 130, 700, 0, 33, 2049], H, Hk, D, bs,
+                                 seed=2600 + bs + H + Hk + D)
+    ok, ov, kt, vt = stored(case)
+    ref = oracle.decode(case.q, kt, vt, case.block_tables, case.context_lens)
+    for grid in (0, 7):
+        dc = DeviceCase(case)
+        dc.store()
+        out = dc.decode(grid_ctas=grid)
+        assert dc.dev_err() == 0
+        got = to_f64(out)
+        assert np.all(np.isfinite(got))
+        assert_close(got, ref, f"decode H={H} Hk={Hk} D={D} bs={bs} grid={grid}")
+        one = DeviceCase(case)
+        o2 = torch.full_like(one.q, float("nan"))
+        pk.pa_decode_step(o2, one.q, one.k_new, one.v_new, one.k_cache, one.v_cache, one.slots,
+                          one.bt, one.ctx, grid_ctas=grid, dev_err=one.err)
+        assert one.dev_err() == 0
+        assert torch.equal(o2.view(torch.int16), out.view(torch.int16))
+        assert torch.equal(one.k_cache.view(torch.int16), dc.k_cache.view(torch.int16))
+        assert torch.equal(one.v_cache.view(torch.int16), dc.v_cache.view(torch.int16))
