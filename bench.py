@@ -698,7 +698,7 @@ def run_ours(args):
     # q, o, block tables, context lengths, slots, and the new rows written to the cache
     step_alg_bytes = kv_bytes + small_bytes + case.slot_mapping.nbytes + store_bytes // 2
     achieved = step_alg_bytes / (step_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(DECODE_SOURCES + ("decode_step.cu",), "decode_step_w2_qwen3_b256.md")
+    traffic = kernel_traffic(DECODE_SOURCES, "decode_step_w2_qwen3_b256.md")
 
     # ---- end to end through the public API with host buffers ---------------------------
     # the step's inputs sit in one pinned host buffer (DecodeStepBuffers) and move with one

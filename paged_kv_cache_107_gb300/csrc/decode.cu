@@ -1,6 +1,7 @@
 // decode.cu — host side of pa_decode: workspace layout, head-slab choice and the
-// launch of the decode kernel (decode_kernel.cuh) without the fused store; head_dim 128
-// with bf16 is instantiated here, the other combinations in decode_d*_*.cu.
+// launch of the decode without the fused store: the CUDA-core kernel (decode_kernel.cuh)
+// for one or two query heads per KV head at head_dim 128 (bf16 here, fp16 in
+// decode_d128_f16.cu), the tensor-core kernel (decode_tc.cu) for every other shape.
 #include "decode_kernel.cuh"
 
 namespace pa {
@@ -15,7 +16,7 @@ int decode_head_slab(int num_kv_heads) {
 bool decode_supported(int num_heads, int num_kv_heads) {
   if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return false;
   const int g = num_heads / num_kv_heads;
-  return g >= 1 && g <= 8;  // 1, 2 on CUDA cores; 3..8 on the tensor-core path
+  return g >= 1 && g <= 8;
 }
 
 int decode_max_ctas(const DeviceInfo& info) { return 4 * info.num_sms; }
@@ -37,10 +38,8 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
 }
 
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
-  if (decode_uses_tc(a.num_heads, a.num_kv_heads)) return launch_decode_tc(a, info, stream);
+  if (decode_uses_tc(a.num_heads, a.num_kv_heads, a.head_dim)) return launch_decode_tc(a, info, stream);
   if (a.head_dim == 128 && !a.f16) return dispatch_slab<false, 128, false>(a, info, stream);
-  if (a.head_dim == 64) return a.f16 ? launch_decode_d64_f16(a, info, stream)
-                                     : launch_decode_d64_bf16(a, info, stream);
   if (a.head_dim == 128) return launch_decode_d128_f16(a, info, stream);
   return PA_ERR_UNSUPPORTED;
 }

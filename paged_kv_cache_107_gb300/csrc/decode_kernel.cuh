@@ -902,6 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++seg_count;
       fence_proxy_async_smem();
     }
+    // order this tile's shared-memory reads before the producer's next copy into the stage
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl.empty[s]);
   }

@@ -1,5 +1,6 @@
-// decode_step_tc.cu — instantiations of the decode step with the fused store on the tensor-core path (decode_tc.cuh): query-head
-// groups of 3 to 8 per KV head, head_dim 64 or 128, bf16 or IEEE fp16 elements.
+// decode_step_tc.cu — instantiations of the decode step with the fused store on the
+// tensor-core path (decode_tc.cuh): every shape the CUDA-core kernel does not take
+// (decode_uses_tc), head_dim 64 or 128, bf16 or IEEE fp16 elements.
 #include "decode_tc.cuh"
 
 namespace pa {

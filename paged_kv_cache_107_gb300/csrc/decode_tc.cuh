@@ -1,4 +1,4 @@
-// decode_tc.cuh — paged decode attention for query-head groups of 3 to 8 per KV head on
+// decode_tc.cuh — paged decode attention for groups of 1 to 8 query heads per KV head on
 // the tensor cores (warp-level mma.sync m16n8k16, bf16 or fp16 operands, fp32 accumulators).
 //
 // Same computation and same work split as decode_kernel.cuh ("nano-vllm解读", sections
@@ -7,7 +7,9 @@
 // is a small dense product: S = Q_j K^T (G x T) and O += P V (G x D). On CUDA cores its dot
 // products, reductions and accumulations outgrow the instruction budget of the HBM stream
 // once G >= 4 (and G = 8 no longer fits in registers); here one warp runs them as
-// 16-row tensor-core products, the G heads padded to 16 rows.
+// 16-row tensor-core products, the G heads padded to 16 rows. The same kernel takes G = 1
+// and 2 wherever its TMA boxes stream faster than the CUDA-core kernel's copies (head_dim
+// 64, slabs narrower than the KV row).
 //
 //  * A stage holds T = 128 / HS tokens of the slab's HS KV heads, K then V, each as D/64
 //    halves laid out [head][token][64 dims]: 128-byte rows with the 128-byte swizzle, so
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int slab = blockIdx.y;
   const int H = a.num_heads;
   const int Hk = a.num_kv_heads;
-  const int G = H / Hk;  // 3..8 on this path
+  const int G = H / Hk;  // 1..8
   const int cap = a.max_blocks * a.block_size;
   const int B = a.num_seqs;
   constexpr int T = TC::T;
@@ -514,6 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         qa[kc][0] = row_ok ? *reinterpret_cast<const uint32_t*>(r0) : 0u;
         qa[kc][1] = row_ok ? *reinterpret_cast<const uint32_t*>(r0 + 16) : 0u;
       }
+      // the slot is released before these loads are used: order them before the next
+      // segment's bulk copy (async proxy) into the slot
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.q_empty[qs]);
       ++q_n;
@@ -769,6 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++seg_count;
       fence_proxy_async_smem();
     }
+    // order this tile's shared-memory reads before the producer's next copy into the stage
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl.empty[s]);
   }

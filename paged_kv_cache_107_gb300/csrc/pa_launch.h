@@ -86,21 +86,23 @@ void decode_workspace_layout(int num_seqs, int num_heads, int num_kv_heads, int 
 int decode_head_slab(int num_kv_heads);
 bool decode_supported(int num_heads, int num_kv_heads);
 int launch_decode(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
-// The decode (and fused-step) instantiations other than head_dim 128 with bf16, one
-// translation unit each.
-int launch_decode_d64_bf16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
-int launch_decode_d64_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
+// The CUDA-core decode (and fused-step) instantiations with fp16 elements, in their own
+// translation units.
 int launch_decode_d128_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
-int launch_decode_step_d64_bf16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
-int launch_decode_step_d64_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
 int launch_decode_step_d128_f16(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
-// Query-head groups of 3 to 8 per KV head: the tensor-core path (decode_tc.cuh).
+// The tensor-core path (decode_tc.cuh).
 int launch_decode_tc(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
 int launch_decode_step_tc(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream);
-// Groups that take the tensor-core path.
-inline bool decode_uses_tc(int num_heads, int num_kv_heads) {
+// Shapes that take the tensor-core path: every group of 3..8 query heads per KV head, and
+// groups of 1 or 2 unless the head dimension is 128 and one slab holds all KV heads
+// (num_kv_heads 1, 2, 4 or 8), the case where a CUDA-core tile is one contiguous run of
+// cache rows. Elsewhere the tensor-core kernel's TMA boxes stream faster.
+inline bool decode_uses_tc(int num_heads, int num_kv_heads, int head_dim) {
   const int g = num_heads / num_kv_heads;
-  return g >= 3 && g <= 8;
+  if (g >= 3) return true;
+  const bool one_slab = num_kv_heads == 1 || num_kv_heads == 2 || num_kv_heads == 4 ||
+                        num_kv_heads == 8;
+  return !(head_dim == 128 && one_slab);
 }
 // The same kernel with the store of token b (k_new/v_new row b) at slot_mapping[b] fused in;
 // the caches are written, so a.k_cache / a.v_cache must point to writable memory.

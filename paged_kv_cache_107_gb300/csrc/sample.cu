@@ -323,6 +323,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(co
     uint4 raw[GPT];
 #pragma unroll
     for (int k = 0; k < GPT; ++k) raw[k] = lds128(tile + ((size_t)k * CT + tid) * 16);
+    // the stage is released before these loads are used: order them before the producer's
+    // next bulk copy (async proxy) into it
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl.empty[st]);  // the tile is in registers
     // scores of this thread's elements, in increasing index order; the tile's maximum is

@@ -172,3 +172,22 @@ def test_tensor_core_block_sizes(bs, H, Hk, D):
         assert torch.equal(o2.view(torch.int16), out.view(torch.int16))
         assert torch.equal(one.k_cache.view(torch.int16), dc.k_cache.view(torch.int16))
         assert torch.equal(one.v_cache.view(torch.int16), dc.v_cache.view(torch.int16))
+
+
+@pytest.mark.parametrize("grid", [3, 20, 152])
+def test_tensor_core_segment_switches(grid):
+    """256 sequences, four in five of them a single tile (G=8, head_dim 128, block_size 16):
+    every CTA switches sequence, and so reloads its Q slot, on almost every tile. Repeated
+    launches must all match the oracle (a Q slot released before its loads complete shows
+    up here as a few wrong rows)."""
+    rng = np.random.default_rng(31)
+    lens = np.where(rng.random(256) < 0.8, rng.integers(1, 17, 256), rng.integers(17, 80, 256))
+    case = workloads.decode_case(lens.tolist(), 64, 8, 128, 16, seed=77)
+    ok, ov, kt, vt = stored(case)
+    ref = oracle.decode(case.q, kt, vt, case.block_tables, case.context_lens)
+    dc = DeviceCase(case)
+    dc.store()
+    for rep in range(12):
+        out = dc.decode(grid_ctas=grid)
+        assert dc.dev_err() == 0
+        assert_close(to_f64(out), ref, f"segment switches grid={grid} launch {rep}")
