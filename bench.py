@@ -59,6 +59,7 @@ def source_sha256(*names) -> str:
 
 
 DECODE_SOURCES = ("decode_kernel.cuh", "pa_device.cuh")
+DECODE_TC_SOURCES = ("decode_tc.cuh", "decode_kernel.cuh", "pa_device.cuh")
 PREFILL_SOURCES = ("prefill_kernel.cuh", "prefill.cu", "umma.cuh", "pa_device.cuh")
 
 
@@ -399,10 +400,12 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128
     return res
 
 
-def measure_variants(dev, steps: int, warmup: int):
+def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
     """head_dim 64 / IEEE fp16 variants on the shapes of the decode step (workload 2: the
     fused store + decode, one launch) and of the chunked prefill (workload 5); and the
-    decode step with 4 and 8 query heads per KV head (the tensor-core path)."""
+    decode step with 4 and 8 query heads per KV head (the tensor-core path). `only` keeps
+    one variant (its tag); `pool_blocks` sizes the 4- and 8-group block pools (at least
+    the 2048 blocks their tables use) for profiler captures."""
     import torch
     import paged_kv_cache_107_gb300 as pk
     from paged_kv_cache_107_gb300 import workloads
@@ -411,11 +414,14 @@ def measure_variants(dev, steps: int, warmup: int):
     for D, dt, tag, heads in ((64, torch.bfloat16, "d64_bf16", 16), (64, torch.float16, "d64_fp16", 16),
                               (128, torch.float16, "d128_fp16", 16), (128, torch.bfloat16, "g4", 32),
                               (128, torch.bfloat16, "g8", 64)):
+        if only is not None and tag != only:
+            continue
         if heads == 16:
             case = workloads.workload(2, poison=True, head_dim=D, dtype=dt)
         else:  # the same lengths and tables with 4 or 8 query heads per KV head
             base = workloads.workload(2, poison=False)
-            case = workloads.decode_case(base.context_lens, heads, 8, D, 256, num_blocks=4096,
+            case = workloads.decode_case(base.context_lens, heads, 8, D, 256,
+                                         num_blocks=pool_blocks or 4096,
                                          seed=107002 + 1000, poison=True, max_blocks=8,
                                          name=f"w2_decode_b256_h{heads}_hk8", dtype=dt)
         tot_ctx, kv_bytes, small_bytes, store_bytes = workload_summary(case)
@@ -451,9 +457,13 @@ def measure_variants(dev, steps: int, warmup: int):
             "workload": case.name, "step_us": ms * 1e3,
             "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
             "achieved_gbs": alg / (ms * 1e-3) / 1e9,
-            "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak}
+            "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak,
+            "alg_bytes_per_launch": alg}
+        if tag == "g8":
+            res["decode_step_" + tag]["traffic"] = kernel_traffic(DECODE_TC_SOURCES,
+                                                                  "decode_tc_g8_w2_b256.md")
         del kc, vc, case
-        if heads == 16:
+        if heads == 16 and only is None:
             res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
                                                     head_dim=D, dtype=dt)
     return res
@@ -797,6 +807,9 @@ def main():
                     help="time only the chunked-prefill step (for profiler captures)")
     ap.add_argument("--variants-only", action="store_true",
                     help="time only the head_dim 64 / fp16 variants")
+    ap.add_argument("--variant", default=None,
+                    choices=["d64_bf16", "d64_fp16", "d128_fp16", "g4", "g8"],
+                    help="with --variants-only: time this variant alone")
     ap.add_argument("--sampler-only", action="store_true",
                     help="time only the Gumbel-max sampler (for profiler captures)")
     ap.add_argument("--pool-blocks", type=int, default=None,
@@ -810,7 +823,8 @@ def main():
         pk.load_library()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        print(json.dumps(measure_variants(dev, args.steps, args.warmup)))
+        print(json.dumps(measure_variants(dev, args.steps, args.warmup, args.variant,
+                                          args.pool_blocks)))
     elif args.sampler_only:
         import torch
         import paged_kv_cache_107_gb300 as pk
