@@ -57,3 +57,93 @@ class DecodeStepBuffers:
         s = stream if stream is not None else torch.cuda.current_stream(self.dev_buf.device)
         with torch.cuda.stream(s):
             self.dev_buf.copy_(self.host_buf, non_blocking=True)
+
+
+class DecodeStepPipeline:
+    """Decode steps whose host<->device copies overlap the neighbouring steps' compute.
+
+    `depth` sets of DecodeStepBuffers and output buffers are used in turn. Step i's inputs
+    move in on an upload stream while step i-1 computes, and its output moves out on a
+    download stream while step i+1 computes; CUDA events keep each buffer's uses in order
+    (a slot's device inputs are overwritten only after the step that read them finished,
+    its device output only after the copy that read it out finished, its pinned host
+    inputs only after their upload finished).
+
+        pipe = DecodeStepPipeline(B, H, Hk, D, max_blocks)
+        for i in range(n):
+            views = pipe.inputs(i)       # pinned host views of step i's inputs
+            ...fill views...
+            pipe.submit(i, run)          # run(dev_views, out) launches step i
+            ...
+            host_out = pipe.output(i)    # step i's output on the host (waits for it)
+    """
+
+    def __init__(self, num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                 max_blocks: int, dtype: torch.dtype = torch.bfloat16, device="cuda",
+                 depth: int = 2, compute_stream=None):
+        if depth < 2:
+            raise ValueError("a pipeline needs at least two buffer sets")
+        self.depth = depth
+        self.device = torch.device(device)
+        self.bufs = [DecodeStepBuffers(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
+                                       dtype=dtype, device=device) for _ in range(depth)]
+        shape = (num_seqs, num_heads, head_dim)
+        self.out_dev = [torch.empty(shape, dtype=dtype, device=device) for _ in range(depth)]
+        self.out_host = [torch.empty(shape, dtype=dtype).pin_memory() for _ in range(depth)]
+        self.compute = (compute_stream if compute_stream is not None
+                        else torch.cuda.current_stream(self.device))
+        self.up = torch.cuda.Stream(self.device)
+        self.down = torch.cuda.Stream(self.device)
+        self.uploaded = [torch.cuda.Event() for _ in range(depth)]
+        self.computed = [torch.cuda.Event() for _ in range(depth)]
+        self.downloaded = [torch.cuda.Event() for _ in range(depth)]
+        self.used = [False] * depth
+        self.h2d_bytes = self.bufs[0].nbytes
+        self.d2h_bytes = self.out_host[0].numel() * self.out_host[0].element_size()
+
+    def inputs(self, i: int) -> Dict[str, torch.Tensor]:
+        """Pinned host views of step i's inputs, free to be written."""
+        k = i % self.depth
+        if self.used[k]:
+            self.uploaded[k].synchronize()
+        return self.bufs[k].host
+
+    def start_after(self, event) -> None:
+        """Make the copy streams wait for `event` (e.g. the start of a timed region)."""
+        self.up.wait_event(event)
+        self.down.wait_event(event)
+
+    def submit(self, i: int, run) -> None:
+        """Upload step i's inputs, run it, and copy its output back, all asynchronously."""
+        k = i % self.depth
+        b = self.bufs[k]
+        if self.used[k]:
+            self.up.wait_event(self.computed[k])         # the last step that read these inputs
+        with torch.cuda.stream(self.up):
+            b.dev_buf.copy_(b.host_buf, non_blocking=True)
+        self.uploaded[k].record(self.up)
+        self.compute.wait_event(self.uploaded[k])
+        if self.used[k]:
+            self.compute.wait_event(self.downloaded[k])  # the last copy out of this output
+        with torch.cuda.stream(self.compute):
+            run(b.dev, self.out_dev[k])
+        self.computed[k].record(self.compute)
+        self.down.wait_event(self.computed[k])
+        with torch.cuda.stream(self.down):
+            self.out_host[k].copy_(self.out_dev[k], non_blocking=True)
+        self.downloaded[k].record(self.down)
+        self.used[k] = True
+
+    def output(self, i: int) -> torch.Tensor:
+        """Step i's output in pinned host memory (valid until step i + depth is submitted)."""
+        k = i % self.depth
+        self.downloaded[k].synchronize()
+        return self.out_host[k]
+
+    def join(self, stream=None) -> None:
+        """Make `stream` (default: the compute stream) wait for every submitted copy."""
+        s = stream if stream is not None else self.compute
+        for k in range(self.depth):
+            if self.used[k]:
+                s.wait_event(self.uploaded[k])
+                s.wait_event(self.downloaded[k])

@@ -206,3 +206,61 @@ def test_step_on_packed_buffers_equals_separate_tensors():
     assert int(err.item()) == 0 and ref_dc.dev_err() == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(kc.view(torch.int16), ref_dc.k_cache.view(torch.int16))
+
+
+def test_pipelined_steps_equal_sequential_steps():
+    """Five decode steps (each sequence one token longer per step, fresh q / k_new / v_new)
+    through DecodeStepPipeline, with uploads and downloads overlapping the neighbouring
+    steps, give step by step the bits of the same five steps run one after another; the
+    caches end equal."""
+    from paged_kv_cache_107_gb300.step_io import DecodeStepPipeline
+    lens0 = [5, 260, 1, 999, 0, 77, 300, 16]
+    B, H, Hk, D, bs, n_steps = len(lens0), 16, 8, 128, 16, 5
+    final = workloads.decode_case([n + n_steps - 1 if n > 0 else 0 for n in lens0], H, Hk, D,
+                                  bs, seed=1900, poison=False)
+    bt = final.block_tables
+    g = torch.Generator().manual_seed(1901)
+    steps = []
+    for i in range(n_steps):
+        lens = np.array([n + i if n > 0 else 0 for n in lens0], np.int32)
+        slots = np.full(B, -1, np.int32)
+        for b in range(B):
+            if lens[b] > 0:
+                pos = int(lens[b]) - 1
+                slots[b] = int(bt[b, pos // bs]) * bs + pos % bs
+        steps.append({"context_lens": torch.from_numpy(lens), "slot_mapping": torch.from_numpy(slots),
+                      "block_tables": torch.from_numpy(bt),
+                      "q": torch.randn((B, H, D), generator=g).to(torch.bfloat16),
+                      "k_new": torch.randn((B, Hk, D), generator=g).to(torch.bfloat16),
+                      "v_new": torch.randn((B, Hk, D), generator=g).to(torch.bfloat16)})
+    kc_a, vc_a = final.k_cache.cuda(), final.v_cache.cuda()
+    kc_b, vc_b = kc_a.clone(), vc_a.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = []
+    for st in steps:
+        o = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
+        d = {k: v.cuda() for k, v in st.items()}
+        pk.pa_decode_step(o, d["q"], d["k_new"], d["v_new"], kc_b, vc_b, d["slot_mapping"],
+                          d["block_tables"], d["context_lens"], dev_err=err)
+        ref.append(o.cpu())
+    pipe = DecodeStepPipeline(B, H, Hk, D, bt.shape[1])
+
+    def run(d, out):
+        pk.pa_decode_step(out, d["q"], d["k_new"], d["v_new"], kc_a, vc_a, d["slot_mapping"],
+                          d["block_tables"], d["context_lens"], dev_err=err)
+
+    got = []
+    for i, st in enumerate(steps):
+        h = pipe.inputs(i)
+        for name, v in st.items():
+            h[name].copy_(v)
+        pipe.submit(i, run)
+        if i >= 1:
+            got.append(pipe.output(i - 1).clone())
+    got.append(pipe.output(n_steps - 1).clone())
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for i, (a, r) in enumerate(zip(got, ref)):
+        assert torch.equal(a.view(torch.int16), r.view(torch.int16)), f"step {i}"
+    assert torch.equal(kc_a.view(torch.int16), kc_b.view(torch.int16))
+    assert torch.equal(vc_a.view(torch.int16), vc_b.view(torch.int16))
