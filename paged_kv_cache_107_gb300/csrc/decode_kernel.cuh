@@ -272,6 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
 
+  // the next kernel on the stream may be scheduled onto SMs as this grid's CTAs leave (it
+  // waits for this grid before touching its results)
+  pdl_launch_dependents();
+
   // ---- prologue: total tiles, then the sequence that holds this CTA's first tile -----
   int64_t local = 0;
   for (int b = tid; b < B; b += kThreads) {
@@ -306,18 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t NT = ctl.nt;
   const int g_eff = ctl.g_eff;
   const int64_t x0 = ctl.x0, x1 = ctl.x1;
-
-  // zero rows of empty (or invalid) sequences assigned to this CTA: one warp per row
-  {
-    const int heads_per_slab = HS * G;
-    for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
-      if (load_ctx(a.context_lens, b, cap) != 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                            ((int64_t)b * H + slab * heads_per_slab) * D);
-      const int nvec = heads_per_slab * D / 8;
-      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
 
   if (x0 < x1) {
     // chunked scan over the sequences until the one holding tile x0 is found
@@ -354,6 +346,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  // everything above read only context_lens (an input no earlier kernel of the step
+  // writes); from here on the kernel reads q, the new rows and the caches and writes out
+  // and the workspace, so the grids launched before it must be complete
+  pdl_wait();
+
+  // zero rows of empty (or invalid) sequences assigned to this CTA: one warp per row
+  {
+    const int heads_per_slab = HS * G;
+    for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
+      if (load_ctx(a.context_lens, b, cap) != 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                            ((int64_t)b * H + slab * heads_per_slab) * D);
+      const int nvec = heads_per_slab * D / 8;
+      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
   // no tiles (all barriers idle; nothing in flight); a start that cannot be located means
   // context_lens changed under the kernel: flag it and do nothing
   if (x0 >= x1) return;
@@ -909,6 +918,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Launch with programmatic stream serialization: the grid may be scheduled while the
+// previous kernel on the stream is still running (its CTAs run the prologue, then wait in
+// pdl_wait for that kernel to complete before using anything it wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 template <int HS, int G, bool FUSED, int D, bool F16>
 int launch_decode_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
   using C = DecCfg<HS, G, D>;
@@ -923,7 +951,9 @@ int launch_decode_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t st
   }
   const int slabs = a.num_kv_heads / HS;
   dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);
-  paged_decode_kernel<HS, G, FUSED, D, F16><<<grid, kThreads, C::SMEM, stream>>>(a);
+  if (launch_dependent(paged_decode_kernel<HS, G, FUSED, D, F16>, grid, dim3(kThreads), C::SMEM,
+                       stream, a) != cudaSuccess)
+    return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -182,6 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl.pb0 = 0;
     fence_mbar_init();
   }
+  // the next kernel on the stream may be scheduled onto SMs as this grid's CTAs leave (it
+  // waits for this grid before touching its results)
+  pdl_launch_dependents();
+
   // ---- prologue: total tiles, then the sequence that holds this CTA's first tile -----
   int64_t local = 0;
   for (int b = tid; b < B; b += kThreads) {
@@ -216,18 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t NT = ctl.nt;
   const int g_eff = ctl.g_eff;
   const int64_t x0 = ctl.x0, x1 = ctl.x1;
-
-  // zero rows of empty (or invalid) sequences assigned to this CTA: one warp per row
-  {
-    const int heads_per_slab = HS * G;
-    for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
-      if (load_ctx(a.context_lens, b, cap) != 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
-                                            ((int64_t)b * H + slab * heads_per_slab) * D);
-      const int nvec = heads_per_slab * D / 8;
-      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
 
   if (x0 < x1) {
     // chunked scan over the sequences until the one holding tile x0 is found
@@ -264,6 +256,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  // everything above read only context_lens (an input no earlier kernel of the step
+  // writes); from here on the kernel reads q, the new rows and the caches and writes out
+  // and the workspace, so the grids launched before it must be complete
+  pdl_wait();
+
+  // zero rows of empty (or invalid) sequences assigned to this CTA: one warp per row
+  {
+    const int heads_per_slab = HS * G;
+    for (int b = c + warp * (int)gridDim.x; b < B; b += (kThreads / 32) * (int)gridDim.x) {
+      if (load_ctx(a.context_lens, b, cap) != 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
+                                            ((int64_t)b * H + slab * heads_per_slab) * D);
+      const int nvec = heads_per_slab * D / 8;
+      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
   // no tiles (all barriers idle; nothing in flight); a start that cannot be located means
   // context_lens changed under the kernel: flag it and do nothing
   if (x0 >= x1) return;
@@ -808,7 +817,9 @@ int launch_decode_tc_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t
     return PA_ERR_CUDA;
   const int slabs = a.num_kv_heads / HS;
   dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);
-  paged_decode_tc_kernel<HS, FUSED, D, F16><<<grid, kThreads, TC::SMEM, stream>>>(mk, mv, a, tb);
+  if (launch_dependent(paged_decode_tc_kernel<HS, FUSED, D, F16>, grid, dim3(kThreads), TC::SMEM,
+                       stream, mk, mv, a, tb) != cudaSuccess)
+    return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -94,6 +94,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// With programmatic stream serialization the next grid may start while this one runs:
+// launch_dependents lets it be scheduled; wait blocks until every grid this one depends
+// on has completed and its memory operations are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
