@@ -235,6 +235,112 @@ __device__ __forceinline__ LaneVec<DPL> zero_lane() {
   return v;
 }
 
+// Last arrival for (sequence b, KV head kvh): combine the partials of the nseg CTAs
+// c_lo.. that processed parts of sequence b, in CTA order, for the G query heads of the
+// group, and write the G output rows. One warp. Lane h + G*j holds the LSE of head h in
+// segment j of a batch of 32/G segments, so the LSEs of every head arrive in one round
+// trip per batch and the per-head maxima come from shuffles; then, segment by segment, the
+// partial outputs of up to four heads are loaded together (one round trip per segment
+// and group of four heads, not one per segment and head). GMAX bounds G.
+template <int D, bool F16, int GMAX>
+__device__ __forceinline__ void combine_partials(const DecodeArgs& a, int b, int kvh, int G,
+                                                 int64_t c_lo, int nseg, int64_t NT, int g_eff,
+                                                 int64_t pb, int lane) {
+  constexpr int CPL = D / 32;                 // combined dims per lane
+  constexpr int HG = GMAX < 4 ? GMAX : 4;     // heads combined together
+  const int H = a.num_heads;
+  const int SB = 32 / G;                      // segments per batch
+  const int my_h = lane % G, my_j = lane / G;
+#pragma unroll 1
+  for (int h0 = 0; h0 < G; h0 += HG) {
+    float acc[HG][CPL], m_h[HG], den[HG];
+#pragma unroll
+    for (int q = 0; q < HG; ++q) {
+      m_h[q] = -INFINITY;
+      den[q] = 0.f;
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) acc[q][e] = 0.f;
+    }
+    for (int s0 = 0; s0 < nseg; s0 += SB) {
+      float ls = -INFINITY;
+      int sl = 0;
+      if (my_j < SB && s0 + my_j < nseg) {
+        const int64_t c2 = c_lo + s0 + my_j;
+        sl = (tile_begin(c2, NT, g_eff) < pb) ? 1 : 0;
+        ls = __ldcg(a.part_lse + (c2 * 2 + sl) * H + kvh * G + my_h);
+      }
+      const int nb = min(SB, nseg - s0);
+      // move each head's running state to the batch maximum
+#pragma unroll
+      for (int q = 0; q < HG; ++q) {
+        if (h0 + q < G) {
+          float bm = -INFINITY;
+          for (int j = 0; j < nb; ++j)
+            bm = fmaxf(bm, __shfl_sync(0xffffffffu, ls, h0 + q + G * j));
+          const float nm = fmaxf(m_h[q], bm);
+          const float al = (m_h[q] == -INFINITY) ? 0.f : fast_exp2(m_h[q] - nm);
+          den[q] *= al;
+#pragma unroll
+          for (int e = 0; e < CPL; ++e) acc[q][e] *= al;
+          m_h[q] = nm;
+        }
+      }
+      for (int j = 0; j < nb; ++j) {
+        const int64_t cj = c_lo + s0 + j;
+        const int slj = __shfl_sync(0xffffffffu, sl, G * j);
+        float w[HG];
+        float po[HG][CPL];
+#pragma unroll
+        for (int q = 0; q < HG; ++q) {
+          w[q] = 0.f;
+#pragma unroll
+          for (int e = 0; e < CPL; ++e) po[q][e] = 0.f;
+          if (h0 + q < G) {
+            const float l = __shfl_sync(0xffffffffu, ls, h0 + q + G * j);
+            w[q] = (m_h[q] == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2(l - m_h[q]);
+            if (w[q] != 0.f) {
+              const float* src =
+                  a.part_o + ((cj * 2 + slj) * H + kvh * G + h0 + q) * D + lane * CPL;
+              if constexpr (CPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                po[q][0] = v.x;
+                po[q][1] = v.y;
+                po[q][2] = v.z;
+                po[q][3] = v.w;
+              } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                po[q][0] = v.x;
+                po[q][1] = v.y;
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < HG; ++q) {
+          den[q] += w[q];
+#pragma unroll
+          for (int e = 0; e < CPL; ++e) acc[q][e] = fmaf(w[q], po[q][e], acc[q][e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < HG; ++q) {
+      if (h0 + q < G) {
+        const float inv = den[q] > 0.f ? 1.f / den[q] : 0.f;
+        uint16_t* dst =
+            static_cast<uint16_t*>(a.out) + ((int64_t)b * H + kvh * G + h0 + q) * D + lane * CPL;
+        if constexpr (CPL == 4) {
+          *reinterpret_cast<uint2*>(dst) =
+              make_uint2(f2_elt2<F16>(acc[q][0] * inv, acc[q][1] * inv),
+                         f2_elt2<F16>(acc[q][2] * inv, acc[q][3] * inv));
+        } else {
+          *reinterpret_cast<uint32_t*>(dst) = f2_elt2<F16>(acc[q][0] * inv, acc[q][1] * inv);
+        }
+      }
+    }
+  }
+}
+
 template <int HS, int G, bool FUSED, int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_decode_kernel(const DecodeArgs a) {
@@ -846,64 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (old == nseg - 1) {
             // (4) last arrival: combine the partials of sequence b in CTA order
             __threadfence();
-#pragma unroll 1
-            for (int hh = 0; hh < G; ++hh) {
-              const int hg = kvh * G + hh;
-              float mx = -INFINITY;
-              for (int k0 = 0; k0 < nseg; k0 += 32) {
-                const int64_t c2 = c_lo + k0 + lane;
-                if (k0 + lane < nseg) {
-                  const int sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
-                  mx = fmaxf(mx, __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg));
-                }
-              }
-#pragma unroll
-              for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-              constexpr int CPL = D / 32;  // combined dims per lane
-              float acc[CPL];
-#pragma unroll
-              for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
-              float den = 0.f;
-              for (int k0 = 0; k0 < nseg; k0 += 32) {
-                const int64_t c2 = c_lo + k0 + lane;
-                float wgt = 0.f;
-                int sl = 0;
-                if (k0 + lane < nseg) {
-                  sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
-                  const float ls = __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg);
-                  wgt = (mx == -INFINITY || ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
-                }
-                const int nk = min(32, nseg - k0);
-                for (int k = 0; k < nk; ++k) {
-                  const float wk = __shfl_sync(0xffffffffu, wgt, k);
-                  const int slk = __shfl_sync(0xffffffffu, sl, k);
-                  const int64_t ck = c_lo + k0 + k;
-                  den += wk;
-                  if (wk != 0.f) {
-                    const float* src = a.part_o + ((ck * 2 + slk) * H + hg) * D + lane * CPL;
-                    if constexpr (CPL == 4) {
-                      const float4 po = __ldcg(reinterpret_cast<const float4*>(src));
-                      acc[0] = fmaf(wk, po.x, acc[0]);
-                      acc[1] = fmaf(wk, po.y, acc[1]);
-                      acc[2] = fmaf(wk, po.z, acc[2]);
-                      acc[3] = fmaf(wk, po.w, acc[3]);
-                    } else {
-                      const float2 po = __ldcg(reinterpret_cast<const float2*>(src));
-                      acc[0] = fmaf(wk, po.x, acc[0]);
-                      acc[1] = fmaf(wk, po.y, acc[1]);
-                    }
-                  }
-                }
-              }
-              const float inv = den > 0.f ? 1.f / den : 0.f;
-              uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)b * H + hg) * D + lane * CPL;
-              if constexpr (CPL == 4) {
-                *reinterpret_cast<uint2*>(dst) = make_uint2(f2_elt2<F16>(acc[0] * inv, acc[1] * inv),
-                                                            f2_elt2<F16>(acc[2] * inv, acc[3] * inv));
-              } else {
-                *reinterpret_cast<uint32_t*>(dst) = f2_elt2<F16>(acc[0] * inv, acc[1] * inv);
-              }
-            }
+            combine_partials<D, F16, G>(a, b, kvh, G, c_lo, nseg, NT, g_eff, meta.pb, lane);
             if (lane == 0) *counter = 0;  // leave the counter zero for the next call
           }
         }
@@ -962,9 +1011,7 @@ int dispatch_group(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t str
   switch (a.num_heads / a.num_kv_heads) {
     case 1: return launch_decode_t<HS, 1, FUSED, D, F16>(a, info, stream);
     case 2: return launch_decode_t<HS, 2, FUSED, D, F16>(a, info, stream);
-    case 4: return launch_decode_t<HS, 4, FUSED, D, F16>(a, info, stream);
-    case 8: return launch_decode_t<HS, 8, FUSED, D, F16>(a, info, stream);
-    default: return PA_ERR_UNSUPPORTED;
+    default: return PA_ERR_UNSUPPORTED;  // larger groups take the tensor-core kernel
   }
 }
 

@@ -718,64 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (old == nseg - 1) {
             // (4) last arrival: combine the partials of sequence b in CTA order
             __threadfence();
-#pragma unroll 1
-            for (int hh = 0; hh < G; ++hh) {
-              const int hg = kvh * G + hh;
-              float mx = -INFINITY;
-              for (int k0 = 0; k0 < nseg; k0 += 32) {
-                const int64_t c2 = c_lo + k0 + lane;
-                if (k0 + lane < nseg) {
-                  const int sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
-                  mx = fmaxf(mx, __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg));
-                }
-              }
-#pragma unroll
-              for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-              constexpr int CPL = D / 32;  // combined dims per lane
-              float acc[CPL];
-#pragma unroll
-              for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
-              float den = 0.f;
-              for (int k0 = 0; k0 < nseg; k0 += 32) {
-                const int64_t c2 = c_lo + k0 + lane;
-                float wgt = 0.f;
-                int sl = 0;
-                if (k0 + lane < nseg) {
-                  sl = (tile_begin(c2, NT, g_eff) < meta.pb) ? 1 : 0;
-                  const float ls = __ldcg(a.part_lse + (c2 * 2 + sl) * H + hg);
-                  wgt = (mx == -INFINITY || ls == -INFINITY) ? 0.f : fast_exp2(ls - mx);
-                }
-                const int nk = min(32, nseg - k0);
-                for (int k = 0; k < nk; ++k) {
-                  const float wk = __shfl_sync(0xffffffffu, wgt, k);
-                  const int slk = __shfl_sync(0xffffffffu, sl, k);
-                  const int64_t ck = c_lo + k0 + k;
-                  den += wk;
-                  if (wk != 0.f) {
-                    const float* src = a.part_o + ((ck * 2 + slk) * H + hg) * D + lane * CPL;
-                    if constexpr (CPL == 4) {
-                      const float4 po = __ldcg(reinterpret_cast<const float4*>(src));
-                      acc[0] = fmaf(wk, po.x, acc[0]);
-                      acc[1] = fmaf(wk, po.y, acc[1]);
-                      acc[2] = fmaf(wk, po.z, acc[2]);
-                      acc[3] = fmaf(wk, po.w, acc[3]);
-                    } else {
-                      const float2 po = __ldcg(reinterpret_cast<const float2*>(src));
-                      acc[0] = fmaf(wk, po.x, acc[0]);
-                      acc[1] = fmaf(wk, po.y, acc[1]);
-                    }
-                  }
-                }
-              }
-              const float inv = den > 0.f ? 1.f / den : 0.f;
-              uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)b * H + hg) * D + lane * CPL;
-              if constexpr (CPL == 4) {
-                *reinterpret_cast<uint2*>(dst) = make_uint2(f2_elt2<F16>(acc[0] * inv, acc[1] * inv),
-                                                            f2_elt2<F16>(acc[2] * inv, acc[3] * inv));
-              } else {
-                *reinterpret_cast<uint32_t*>(dst) = f2_elt2<F16>(acc[0] * inv, acc[1] * inv);
-              }
-            }
+            combine_partials<D, F16, kTcGMax>(a, b, kvh, G, c_lo, nseg, NT, g_eff, meta.pb, lane);
             if (lane == 0) *counter = 0;  // leave the counter zero for the next call
           }
         }
