@@ -61,7 +61,11 @@ struct TcCtrl {
 
 template <int HS, int D>
 struct TcCfg {
-  static constexpr int T = 128 / HS;               // tokens per stage (8 warps x 16 / HS)
+  // a warp takes SUB blocks of 16 tokens per stage: two at head_dim 64, so that a stage
+  // carries as many bytes as at head_dim 128 and the per-stage costs (barriers, block
+  // lookups, copies) are spread over twice the tokens
+  static constexpr int SUB = D == 64 ? 2 : 1;
+  static constexpr int T = 128 * SUB / HS;         // tokens per stage (8 warps x 16 x SUB / HS)
   static constexpr int WPH = kConsumerWarps / HS;  // warps per KV head (token split)
   static constexpr int NH = D / 64;                // 64-dim halves of a head row
   static constexpr int HALF = HS * T * 128;        // bytes of one half: [head][token][64 dims]
@@ -477,19 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [head][token]; chunk c of the row sits at chunk c ^ (t % 8)
   const int tbl = tb > 0 ? tb : T;
   const int lg_tbl = __ffs(tbl) - 1;
-  const int tw0 = w * 16;  // this warp's first token of the tile
+  const int tw_base = w * 16 * TC::SUB;  // this warp's first token of the tile
   auto row_off = [&](int t) -> int {
     return ((((t >> lg_tbl) * HS + j) << lg_tbl) + (t & (tbl - 1))) * 128;
   };
-  const int tK = tw0 + (lane & 7) + ((lane >> 4) << 3);        // ldmatrix row (K, S product)
-  const int tV = tw0 + (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row (V, trans)
-  const int sw = lane & 7;                                   // = t % 8 of both rows
+  const int sw = lane & 7;                                   // = t % 8 of the ldmatrix rows
   const int k_hi = (lane >> 3) & 1, v_hi = lane >> 4;        // second 8 dims of a 16-dim chunk
   // byte offsets within a stage: 16-byte chunk c = 2*(chunk16 % 4) + hi of a 128-byte row sits
   // at (c ^ sw) * 16 = ((chunk16 % 4) * 32 ^ (sw & 6) * 16) + (hi ^ (sw & 1)) * 16
   const uint32_t x_sw = (uint32_t)(sw & 6) << 4;
-  const uint32_t k_lane = (uint32_t)row_off(tK) + ((uint32_t)(k_hi ^ (sw & 1)) << 4);
-  const uint32_t v_lane = (uint32_t)(TC::KV_BYTES + row_off(tV)) + ((uint32_t)(v_hi ^ (sw & 1)) << 4);
   const uint32_t ks_lane = (uint32_t)(2 * TC::KV_BYTES + (j * D + k_hi * 8) * 2);
   const uint32_t vs_lane = (uint32_t)(2 * TC::KV_BYTES + TC::SIDE_ROW + (j * D + v_hi * 8) * 2);
   const uint32_t smem_base = smem_u32(smem);
@@ -537,89 +537,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_part = 0.f;
     }
 
-    // rows of this warp's V past the tile's valid tokens: zero them (head j's rows)
-    if (tw0 + 16 > count) {
-      for (int i = lane; i < 16 * TC::NH * 8; i += 32) {
-        const int t = tw0 + i / (TC::NH * 8);
-        if (t >= count)
-          *reinterpret_cast<uint4*>(Vst + ((i >> 3) % TC::NH) * TC::HALF + row_off(t) + (i & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < TC::SUB; ++u) {
+      const int tw0 = tw_base + u * 16;  // first token of this 16-token block
+      const int tK = tw0 + (lane & 7) + ((lane >> 4) << 3);        // ldmatrix row (K, S product)
+      const int tV = tw0 + (lane & 7) + (((lane >> 3) & 1) << 3);  // ldmatrix row (V, trans)
+      const uint32_t k_lane = (uint32_t)row_off(tK) + ((uint32_t)(k_hi ^ (sw & 1)) << 4);
+      const uint32_t v_lane =
+          (uint32_t)(TC::KV_BYTES + row_off(tV)) + ((uint32_t)(v_hi ^ (sw & 1)) << 4);
+      // rows of this warp's V past the tile's valid tokens: zero them (head j's rows)
+      if (tw0 + 16 > count) {
+        for (int i = lane; i < 16 * TC::NH * 8; i += 32) {
+          const int t = tw0 + i / (TC::NH * 8);
+          if (t >= count)
+            *reinterpret_cast<uint4*>(Vst + ((i >> 3) % TC::NH) * TC::HALF + row_off(t) + (i & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-    bool k_new_lane = false, v_new_lane = false;
-    if constexpr (FUSED) {
-      // the new token's row of KV head kvh: from the side rows to its cache slot
-      if (meta.new_row >= tw0 && meta.new_row < tw0 + 16) {
-        const int64_t dst = meta.new_slot * ((int64_t)Hk * D) + (int64_t)kvh * D;
-        const int half = lane >> 4, sub = lane & 15;
-        if (sub < D / 8) {
-          const unsigned char* srcp = side + half * TC::SIDE_ROW + j * D * 2 + sub * 16;
-          uint16_t* cache = static_cast<uint16_t*>(const_cast<void*>(half ? a.v_cache : a.k_cache));
-          *reinterpret_cast<uint4*>(cache + dst + sub * 8) = *reinterpret_cast<const uint4*>(srcp);
+      bool k_new_lane = false, v_new_lane = false;
+      if constexpr (FUSED) {
+        // the new token's row of KV head kvh: from the side rows to its cache slot
+        if (meta.new_row >= tw0 && meta.new_row < tw0 + 16) {
+          const int64_t dst = meta.new_slot * ((int64_t)Hk * D) + (int64_t)kvh * D;
+          const int half = lane >> 4, sub = lane & 15;
+          if (sub < D / 8) {
+            const unsigned char* srcp = side + half * TC::SIDE_ROW + j * D * 2 + sub * 16;
+            uint16_t* cache = static_cast<uint16_t*>(const_cast<void*>(half ? a.v_cache : a.k_cache));
+            *reinterpret_cast<uint4*>(cache + dst + sub * 8) = *reinterpret_cast<const uint4*>(srcp);
+          }
+        }
+        k_new_lane = tK == meta.new_row;
+        v_new_lane = tV == meta.new_row;
+      }
+
+      // ---- S = Q K^T for 16 tokens: two 8-token column tiles ----------------------------
+      float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // row gid, tokens 8n + 2tig, +1
+      const uint32_t st_u = smem_base + (uint32_t)s * TC::STAGE_BYTES;
+      {
+  #pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+          uint32_t r[4];
+          uint32_t kp = st_u + k_lane + (kc >> 2) * TC::HALF + (((uint32_t)(kc & 3) << 5) ^ x_sw);
+          if constexpr (FUSED) kp = k_new_lane ? st_u + ks_lane + kc * 32 : kp;
+          ldsm_x4(r, kp);
+          mma16816<F16>(sc[0][0], sc[0][1], z, qa[kc][0], qa[kc][1], r[0], r[1]);
+          mma16816<F16>(sc[1][0], sc[1][1], z, qa[kc][0], qa[kc][1], r[2], r[3]);
         }
       }
-      k_new_lane = tK == meta.new_row;
-      v_new_lane = tV == meta.new_row;
-    }
+      // ---- online softmax in the accumulator layout (a row's scores sit in one quad) -----
+      float tmax = -INFINITY;
+  #pragma unroll
+      for (int n = 0; n < 2; ++n)
+  #pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = tw0 + n * 8 + 2 * tig + e;
+          const float v = t < count ? sc[n][e] * sl2 : -INFINITY;
+          sc[n][e] = v;
+          tmax = fmaxf(tmax, v);
+        }
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float m_new = fmaxf(m_run, tmax);
+      const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
+      m_run = m_new;
+      float p[2][2];
+  #pragma unroll
+      for (int n = 0; n < 2; ++n)
+  #pragma unroll
+        for (int e = 0; e < 2; ++e) p[n][e] = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[n][e] - m_new);
+      l_part = l_part * alpha + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+  #pragma unroll
+        for (int n = 0; n < NO; ++n) {
+          o[n][0] *= alpha;
+          o[n][1] *= alpha;
+        }
+      }
+      // ---- O += P V: P (row gid x 16 tokens) straight from the S accumulators ------------
+      const uint32_t pa0 = f2_elt2<F16>(p[0][0], p[0][1]);  // tokens 2tig, +1
+      const uint32_t pa2 = f2_elt2<F16>(p[1][0], p[1][1]);  // tokens 8 + 2tig, +1
+      {
+  #pragma unroll
+        for (int dn = 0; dn < D / 16; ++dn) {
+          uint32_t r[4];
+          uint32_t vp = st_u + v_lane + (dn >> 2) * TC::HALF + (((uint32_t)(dn & 3) << 5) ^ x_sw);
+          if constexpr (FUSED) vp = v_new_lane ? st_u + vs_lane + dn * 32 : vp;
+          ldsm_x4_t(r, vp);
+          mma16816<F16>(o[2 * dn][0], o[2 * dn][1], z, pa0, pa2, r[0], r[1]);
+          mma16816<F16>(o[2 * dn + 1][0], o[2 * dn + 1][1], z, pa0, pa2, r[2], r[3]);
+        }
+      }
 
-    // ---- S = Q K^T for 16 tokens: two 8-token column tiles ----------------------------
-    float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // row gid, tokens 8n + 2tig, +1
-    const uint32_t st_u = smem_base + (uint32_t)s * TC::STAGE_BYTES;
-    {
-#pragma unroll
-      for (int kc = 0; kc < KC; ++kc) {
-        uint32_t r[4];
-        uint32_t kp = st_u + k_lane + (kc >> 2) * TC::HALF + (((uint32_t)(kc & 3) << 5) ^ x_sw);
-        if constexpr (FUSED) kp = k_new_lane ? st_u + ks_lane + kc * 32 : kp;
-        ldsm_x4(r, kp);
-        mma16816<F16>(sc[0][0], sc[0][1], z, qa[kc][0], qa[kc][1], r[0], r[1]);
-        mma16816<F16>(sc[1][0], sc[1][1], z, qa[kc][0], qa[kc][1], r[2], r[3]);
-      }
-    }
-    // ---- online softmax in the accumulator layout (a row's scores sit in one quad) -----
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = tw0 + n * 8 + 2 * tig + e;
-        const float v = t < count ? sc[n][e] * sl2 : -INFINITY;
-        sc[n][e] = v;
-        tmax = fmaxf(tmax, v);
-      }
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-    const float m_new = fmaxf(m_run, tmax);
-    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-    m_run = m_new;
-    float p[2][2];
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) p[n][e] = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[n][e] - m_new);
-    l_part = l_part * alpha + (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int n = 0; n < NO; ++n) {
-        o[n][0] *= alpha;
-        o[n][1] *= alpha;
-      }
-    }
-    // ---- O += P V: P (row gid x 16 tokens) straight from the S accumulators ------------
-    const uint32_t pa0 = f2_elt2<F16>(p[0][0], p[0][1]);  // tokens 2tig, +1
-    const uint32_t pa2 = f2_elt2<F16>(p[1][0], p[1][1]);  // tokens 8 + 2tig, +1
-    {
-#pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        uint32_t r[4];
-        uint32_t vp = st_u + v_lane + (dn >> 2) * TC::HALF + (((uint32_t)(dn & 3) << 5) ^ x_sw);
-        if constexpr (FUSED) vp = v_new_lane ? st_u + vs_lane + dn * 32 : vp;
-        ldsm_x4_t(r, vp);
-        mma16816<F16>(o[2 * dn][0], o[2 * dn][1], z, pa0, pa2, r[0], r[1]);
-        mma16816<F16>(o[2 * dn + 1][0], o[2 * dn + 1][1], z, pa0, pa2, r[2], r[3]);
-      }
     }
 
     if (meta.flags & kFlagLast) {
