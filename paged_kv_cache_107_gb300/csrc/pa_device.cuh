@@ -94,6 +94,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- dependent launches
 // With programmatic stream serialization the next grid may start while this one runs:
 // launch_dependents lets it be scheduled; wait blocks until every grid this one depends
