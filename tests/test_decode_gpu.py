@@ -64,9 +64,9 @@ def test_context_edges(lens, bs):
                                   (8, 4), (16, 4), (4, 2), (8, 2), (2, 1), (8, 1), (24, 8),
                                   (40, 8), (48, 8), (56, 8), (12, 4), (5, 1), (14, 2), (32, 2)])
 def test_head_layouts(H, Hk):
-    """GQA group sizes 1..8 (1 and 2 on CUDA cores, 3..8 on the tensor-core path; 16 is
-    rejected) and KV head slabs of 8, 4, 2, 1 heads (the slab path with several warps per
-    KV head merges their softmax states)."""
+    """GQA group sizes 1..8 (1 and 2 on CUDA cores when one slab holds every KV head, all
+    other layouts on the tensor-core path; 16 is rejected) and KV head slabs of 8, 4, 2, 1
+    heads (the slab path with several warps per KV head merges their softmax states)."""
     case = workloads.decode_case([1, 40, 300, 129], H, Hk, 128, 16, seed=500 + H * 7 + Hk)
     if not 1 <= (H // Hk) <= 8:
         with pytest.raises(pk.PagedAttentionError):
