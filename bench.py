@@ -449,6 +449,15 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
             step()
             b.record(stream)
         torch.cuda.synchronize(dev)
+        # the same steps back to back, no events between them (each launch a dependent of
+        # the one before, as in a decode loop)
+        lo, hi = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lo.record(stream)
+        for _ in range(steps):
+            step()
+        hi.record(stream)
+        torch.cuda.synchronize(dev)
+        loop_ms = lo.elapsed_time(hi) / steps
         if int(err.item()) != 0:
             raise RuntimeError(f"device error bits {int(err.item())} in the {tag} step")
         ms = statistics.median(a.elapsed_time(b) for a, b in ev)
@@ -458,7 +467,9 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
             "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9,
             "achieved_gbs": alg / (ms * 1e-3) / 1e9,
             "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak,
-            "alg_bytes_per_launch": alg}
+            "alg_bytes_per_launch": alg,
+            "loop_step_us": loop_ms * 1e3,
+            "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9}
         if tag == "g8":
             res["decode_step_" + tag]["traffic"] = kernel_traffic(DECODE_TC_SOURCES,
                                                                   "decode_tc_g8_w2_b256.md")

@@ -260,6 +260,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  // Before waiting, the producer warp warms L2 with the K/V runs of this CTA's first
+  // tiles (lanes 2t, 2t+1: K, V of tile t), as the CUDA-core kernel does; only when the
+  // slab is every KV head, so that a tile inside one block is one run of cache rows.
+  if (warp == kProducerWarp && x0 < x1 && ctl.found && lane < 2 * S) {
+    const int64_t row_elems = (int64_t)Hk * D;
+    if (slab == 0 && Hk == HS && x0 + (lane >> 1) < x1) {
+      const int64_t x = x0 + (lane >> 1);
+      int b = ctl.b0;
+      int64_t pb = ctl.pb0;
+      int ctx_b = load_ctx(a.context_lens, b, cap);
+      int nb = (ctx_b + T - 1) / T;
+      while (x >= pb + nb && b + 1 < B) {
+        pb += nb;
+        ++b;
+        ctx_b = load_ctx(a.context_lens, b, cap);
+        nb = (ctx_b + T - 1) / T;
+      }
+      const int tok0 = (int)(x - pb) * T;
+      const int count = min(T, ctx_b - tok0);
+      if (count > 0 && tok0 / a.block_size == (tok0 + count - 1) / a.block_size) {
+        const int blk = __ldg(a.block_tables + (int64_t)b * a.max_blocks + tok0 / a.block_size);
+        if (blk >= 0 && (int64_t)blk < a.num_blocks) {
+          const uint16_t* base = static_cast<const uint16_t*>((lane & 1) ? a.v_cache : a.k_cache);
+          const uint16_t* src = base + ((int64_t)blk * a.block_size + tok0 % a.block_size) * row_elems;
+          prefetch_l2_bulk(src, (uint32_t)(count * row_elems * 2));
+        }
+      }
+    }
+  }
   // everything above read only context_lens (an input no earlier kernel of the step
   // writes); from here on the kernel reads q, the new rows and the caches and writes out
   // and the workspace, so the grids launched before it must be complete
