@@ -264,3 +264,25 @@ def test_pipelined_steps_equal_sequential_steps():
         assert torch.equal(a.view(torch.int16), r.view(torch.int16)), f"step {i}"
     assert torch.equal(kc_a.view(torch.int16), kc_b.view(torch.int16))
     assert torch.equal(vc_a.view(torch.int16), vc_b.view(torch.int16))
+
+
+def test_context_lens_written_by_the_kernel_just_before():
+    """The step reads context_lens before it waits for the kernel launched ahead of it on
+    the stream. An ordinary kernel lets its dependents start only when it completes, so
+    context_lens written by such a kernel right before the step must be the ones used:
+    the lengths start out wrong (all 1) and an elementwise kernel on the same stream writes
+    the right ones just before each launch."""
+    case = workloads.decode_case([300, 17, 1024, 65, 2000, 3], 16, 8, 128, 16, seed=1950,
+                                 poison=False)
+    ok, ov = oracle_after_store(case)
+    ref = oracle.decode(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+                        case.context_lens)
+    right = torch.from_numpy(case.context_lens).cuda()
+    for rep in range(4):
+        dc = DeviceCase(case)
+        dc.ctx.fill_(1)
+        torch.cuda.synchronize()
+        torch.add(right, 0, out=dc.ctx)  # a kernel on the stream, immediately before
+        out = fused(dc)
+        assert dc.dev_err() == 0
+        assert_close(to_f64(out), ref, f"lengths written just before, launch {rep}")
