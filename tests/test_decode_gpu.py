@@ -83,15 +83,21 @@ def test_empty_rows_are_zero():
     assert np.all(o[[0, 2, 3]] == 0.0)
 
 
-def test_run_to_run_bitwise_deterministic():
-    case = workloads.decode_case(list(np.random.default_rng(7).integers(1, 3000, 64)), 16, 8,
-                                 128, 256, seed=601, num_blocks=1024)
+@pytest.mark.parametrize("H,Hk,D", [(16, 8, 128), (64, 8, 128), (28, 4, 128), (32, 16, 128),
+                                    (16, 8, 64)])
+@pytest.mark.parametrize("grid", [0, 7])
+def test_run_to_run_bitwise_deterministic(H, Hk, D, grid):
+    """The split combine uses the arrival counters only to pick the CTA that combines, in
+    CTA order, so repeated launches give the same bits (both decode kernels)."""
+    case = workloads.decode_case(list(np.random.default_rng(7).integers(1, 3000, 64)), H, Hk,
+                                 D, 256, seed=601, num_blocks=1024)
     dc = DeviceCase(case)
     dc.store()
-    a = dc.decode()
-    b = dc.decode()
-    c = dc.decode()
+    a = dc.decode(grid_ctas=grid)
+    b = dc.decode(grid_ctas=grid)
+    c = dc.decode(grid_ctas=grid)
     torch.cuda.synchronize()
+    assert dc.dev_err() == 0
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 

@@ -286,3 +286,15 @@ def test_context_lens_written_by_the_kernel_just_before():
         out = fused(dc)
         assert dc.dev_err() == 0
         assert_close(to_f64(out), ref, f"lengths written just before, launch {rep}")
+
+
+@pytest.mark.parametrize("H,Hk", [(16, 8), (64, 8), (28, 4)])
+def test_many_short_sequences(H, Hk):
+    """4096 sequences of 1..64 tokens (block_size 16): dozens of sequences per CTA, most of
+    them whole, the rest cut at CTA boundaries; the fused step against the oracle on 4096
+    sampled rows, and every cache byte."""
+    rng = np.random.default_rng(1960 + H + Hk)
+    lens = rng.integers(1, 65, size=4096)
+    case = workloads.decode_case(lens.tolist(), H, Hk, 128, 16, seed=1961 + H, poison=True)
+    pairs = np.sort(rng.choice(case.num_seqs * case.num_heads, 4096, replace=False))
+    run_step(case, pairs=pairs)
