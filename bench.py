@@ -477,6 +477,75 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
         if heads == 16 and only is None:
             res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
                                                     head_dim=D, dtype=dt)
+    if only is None:
+        res["decode_step_block_sizes"] = measure_block_sizes(dev, min(steps, 30), warmup)
+    return res
+
+
+def measure_block_sizes(dev, steps: int, warmup: int):
+    """The fused decode step on the decode-step lengths (B=256, ctx U{100..2048}, H=16,
+    H_kv=8, D=128) for block sizes 16..256: one launch at a time and back to back. Cache
+    contents are made on the device (the parity tests cover these block sizes)."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_107_gb300 as pk
+    B, H, Hk, D = 256, 16, 8, 128
+    res = {}
+    for bs in (16, 32, 64, 128, 256):
+        rng = np.random.default_rng(107002)
+        lens = rng.integers(100, 2048 + 1, size=B).astype(np.int32)
+        nblk = (lens + bs - 1) // bs
+        nb = int(nblk.sum())
+        perm = rng.permutation(nb).astype(np.int32)
+        bt = np.full((B, int(nblk.max())), -1, np.int32)
+        o = 0
+        for b in range(B):
+            bt[b, :nblk[b]] = perm[o:o + nblk[b]]
+            o += nblk[b]
+        pos = lens - 1
+        slots = (bt[np.arange(B), pos // bs].astype(np.int64) * bs + pos % bs).astype(np.int32)
+        g = torch.Generator(device=dev)
+        g.manual_seed(107002 + bs)
+        kc = torch.randn((nb, bs, Hk, D), generator=g, device=dev).to(torch.bfloat16)
+        vc = torch.randn((nb, bs, Hk, D), generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn((B, H, D), generator=g, device=dev).to(torch.bfloat16)
+        kn = torch.randn((B, Hk, D), generator=g, device=dev).to(torch.bfloat16)
+        vn = torch.randn((B, Hk, D), generator=g, device=dev).to(torch.bfloat16)
+        sd = torch.from_numpy(slots).to(dev)
+        btd = torch.from_numpy(bt).to(dev)
+        ctx = torch.from_numpy(lens).to(dev)
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = pk.DecodeWorkspace(B, H, Hk, D, device=dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def step():
+            pk.pa_decode_step(out, q, kn, vn, kc, vc, sd, btd, ctx, workspace=ws, dev_err=err,
+                              stream=stream)
+
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        lo, hi = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lo.record(stream)
+        for _ in range(steps):
+            step()
+        hi.record(stream)
+        torch.cuda.synchronize(dev)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item())} at block size {bs}")
+        kv = int(lens.sum()) * Hk * D * 2 * 2
+        per = statistics.median(a.elapsed_time(b) for a, b in ev)
+        loop = lo.elapsed_time(hi) / steps
+        res[f"bs{bs}"] = {"step_us": per * 1e3, "loop_step_us": loop * 1e3,
+                          "loop_kv_gbs": kv / (loop * 1e-3) / 1e9}
+        del kc, vc
     return res
 
 
