@@ -24,10 +24,18 @@
 //    the cache), and the half-warp that loads the row from shared memory also writes it to
 //    the cache slot. Store and attention are one launch, and the new row is read once.
 //  * One CTA handles a slab of HS KV heads (all of them when H_kv <= 8), so one token's
-//    rows for the slab are HS*256 contiguous bytes: the producer warp moves each token row
-//    with one cp.async.bulk (TMA engine) into a STAGES-deep shared-memory ring guarded by
-//    mbarriers. Tiles never need block alignment: each token's row is addressed through
-//    the block table on its own.
+//    rows for the slab are HS*256 contiguous bytes: the producer warp moves a tile's rows
+//    into a STAGES-deep shared-memory ring guarded by mbarriers, with one cp.async.bulk
+//    (TMA engine) per K and V when they form one run of cache rows (the slab is every KV
+//    head and the tile lies in one block), else one per token row. Tiles never need block
+//    alignment: each token's row can be addressed through the block table on its own.
+//  * Launched as a programmatic dependent of the previous kernel on the stream: the
+//    prologue reads only context_lens, the producer prefetches its first tiles' K/V runs
+//    into L2, and everything that reads q, the new rows or the caches, or writes the
+//    output or the workspace, waits for the previous grid first.
+//  * The last CTA of a split sequence combines the partials in CTA order
+//    (combine_partials): the LSEs of every head and segment in one round trip per batch,
+//    the partial outputs of up to four heads per segment together.
 //  * 8 consumer warps (+1 producer warp: 9 warps keep 168 registers per thread):
 //    warp (j, w) owns KV head j of the slab and 16 tokens of every tile; a half-warp
 //    holds one token row (16 lanes x 16 bytes), so each K row is read from shared memory

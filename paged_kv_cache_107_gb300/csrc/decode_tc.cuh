@@ -11,17 +11,21 @@
 // and 2 wherever its TMA boxes stream faster than the CUDA-core kernel's copies (head_dim
 // 64, slabs narrower than the KV row).
 //
-//  * A stage holds T = 128 / HS tokens of the slab's HS KV heads, K then V, each as D/64
-//    halves laid out [head][token][64 dims]: 128-byte rows with the 128-byte swizzle, so
-//    the 8 token rows an ldmatrix reads sit in 8 different bank groups. The producer fills
-//    it with TMA boxes of tb tokens x HS heads x 64 dims (tb = the largest power of two
-//    dividing block_size, at most T), i.e. 2 * D/64 * T/tb copies per stage; a block size
-//    with no such tb >= 8 is filled with 16-byte cp.async copies into the same layout.
+//  * A stage holds T = 128 * SUB / HS tokens of the slab's HS KV heads (SUB = 2 at head_dim
+//    64, else 1, so that a stage always carries 64 KB), K then V, each as D/64 halves laid
+//    out [head][token][64 dims]: 128-byte rows with the 128-byte swizzle, so the 8 token
+//    rows an ldmatrix reads sit in 8 different bank groups. The producer fills it with TMA
+//    boxes of tb tokens x HS heads x 64 dims (tb = the largest power of two dividing
+//    block_size, at most T), i.e. 2 * D/64 * T/tb copies per stage; a block size with no
+//    such tb >= 8 is filled with 16-byte cp.async copies into the same layout.
+//  * Launched as a programmatic dependent (decode_kernel.cuh's launch_dependent): the
+//    prologue reads only context_lens; before waiting for the previous grid the producer
+//    prefetches its first tiles' K/V runs into L2.
 //  * The fused step's new token: its K and V rows of the slab come from k_new / v_new into
 //    a side row of the stage; lanes whose token is the new one point ldmatrix there.
 //  * Q of a segment goes to its own slot (two where shared memory allows), loaded once per
 //    sequence and released as soon as every warp holds its fragments.
-//  * Warp (j, w): KV head j of the slab, tokens 16w..16w+15 of each tile. S: for every
+//  * Warp (j, w): KV head j of the slab, SUB blocks of 16 tokens of each tile. S: for every
 //    16-dim chunk, ldmatrix.x4 gives the K fragments of two 8-token column tiles. Online
 //    softmax in the accumulator layout (a row's 16 scores sit in one quad of lanes); the S
 //    accumulators become the A operand of O += P V directly; V fragments come from
