@@ -65,10 +65,11 @@ __device__ __forceinline__ void philox4x32_10(uint32_t& c0, uint32_t& c1, uint32
 
 // -log2(u) for u = (2k + 1) / 2^24, k the top 23 bits of `bits`, with relative accuracy
 // over the whole range. u = (1 + k/2^23) - (1 - 2^-24) and w = 1 - u =
-// (1 + (2^23 - 1 - k)/2^23) - (1 - 2^-24) are both exact in binary32. For u < 1/2 the
-// hardware log2 (|log2 u| >= 1, so its absolute error is a small relative one); for
-// u >= 1/2, -log2(1 - w) = (2 / ln 2) atanh(s) with s = w / (2 - w) <= 1/3, summed by the
-// Taylor series of atanh up to s^11 (truncation below 1.5e-7 relative).
+// (1 + (2^23 - 1 - k)/2^23) - (1 - 2^-24) are both exact in binary32. For u <= 0.9 the
+// hardware log2 (absolute error about 2^-22 on [1/2, 2], and |log2 u| >= 0.15, so at most
+// about 2e-6 relative); for u > 0.9, -log2(1 - w) = (2 / ln 2) atanh(s) with
+// s = w / (2 - w) < 0.053, summed by the Taylor series of atanh up to s^5 (truncation below
+// 1e-8 relative).
 __device__ __forceinline__ float neg_log2_uniform(uint32_t bits) {
   const uint32_t k = bits >> 9;
   const float u = __uint_as_float(0x3F800000u | k) - 0.99999994039535522f;
@@ -78,13 +79,11 @@ __device__ __forceinline__ float neg_log2_uniform(uint32_t bits) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(2.f - w));
   const float s = w * r;
   const float s2 = s * s;
-  float p = 0.26230818925253880f;         // (2 / ln 2) / 11
-  p = fmaf(p, s2, 0.32059889797532520f);  // (2 / ln 2) / 9
-  p = fmaf(p, s2, 0.41219858311113240f);  // (2 / ln 2) / 7
-  p = fmaf(p, s2, 0.57707801635558540f);  // (2 / ln 2) / 5
+  float p = 0.57707801635558540f;         // (2 / ln 2) / 5
   p = fmaf(p, s2, 0.96179669392597560f);  // (2 / ln 2) / 3
   p = fmaf(p, s2, 2.88539008177792680f);  // 2 / ln 2
-  return k < (1u << 22) ? a : s * p;
+  // u <= 0.9 exactly when k <= 7549746 (u = (2k + 1) / 2^24)
+  return k <= 7549746u ? a : s * p;
 }
 
 // Ranking score of one element in log2 units: l * (log2(e) / T) - log2(-log2 u).

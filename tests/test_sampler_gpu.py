@@ -1,8 +1,9 @@
 """GPU parity of pa_gumbel_sample against the fp64 oracle ("nano-vllm解读", "Gumbel-Max采样";
 "Model Runner V2 设计文档", section 6 "Gumbel 采样内核").
 
-The kernel decides in fp32 (logit * (1/T) + noise, the noise from CUDA's logf and the
-hardware log2), the oracle in fp64 from the same 32-bit random words. So a row must give
+The kernel decides in fp32 (logit * log2(e)/T + noise, the noise from the hardware log2
+and, for u > 0.9, an atanh series on the exact 1 - u), the oracle in fp64 from the same
+32-bit random words. So a row must give
 exactly the oracle's index whenever the oracle's best score leads the runner-up by more
 than the fp32 error bound TOL; inside that bound (a near-tie, where both indices are
 correct samples) the kernel's choice must be one of the near-best scores."""
