@@ -104,3 +104,30 @@ def test_validation_without_launch(lib):
     rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 1, 256,
                                ctypes.c_int64(4), 1, ctypes.c_float(0), None, None)
     assert rc in (2, 3)
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/pa.h compiles as C99 with every warning an error, and a C program that takes
+    the address of every declared function links against the library: the boundary
+    needs no C++ and no torch."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "uses_pa.c"
+    body = "\n".join(f"  fns[{i}] = (void (*)(void)){n};" for i, n in enumerate(names))
+    src.write_text('#include "pa.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n"
+                   f"  void (*fns[{len(names)}])(void);\n{body}\n"
+                   f"  printf(\"%s %d\\n\", pa_status_str(PA_OK), {len(names)});\n"
+                   "  return fns[0] == 0;\n}\n")
+    exe = tmp_path / "uses_pa"
+    libdir = os.path.dirname(lib_build.LIB_PATH)
+    libname = os.path.basename(lib_build.LIB_PATH)[3:-3]  # libX.so -> X
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+           "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+           "-L", libdir, f"-l{libname}", f"-Wl,-rpath,{libdir}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
