@@ -254,10 +254,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  * Launch: a programmatic dependent launch. The grid may start while the previous kernel
  * on the stream is still running, provided that kernel lets its dependents start early
  * (griddepcontrol.launch_dependents); an ordinary kernel does so only when it completes.
- * Before waiting for that kernel the grid reads context_lens (pa_decode_step also reads
+ * Before waiting for that kernel the grid reads context_lens and the block_tables rows of
+ * its first tiles (to prefetch those tiles into L2; pa_decode_step also reads
  * slot_mapping); everything else is read and every output written after the wait. So
- * context_lens and slot_mapping must not be written by a preceding kernel that releases
- * its dependents before it has written them (host copies and ordinary kernels are fine).
+ * context_lens, block_tables and slot_mapping must not be written by a preceding kernel
+ * that releases its dependents before it has written them (host copies and ordinary
+ * kernels are fine; of this library's kernels only the decode kernels release early, and
+ * they write none of these).
  */
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
@@ -300,8 +303,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  * the cache. Rows of other sequences that alias the new token's slot (never the case when
  * the slot's block holds the newest position of only one sequence) race with the store.
  * Graph-capturable: no host synchronisation, no allocation, fixed grid for any batch.
- * Launched as a programmatic dependent, with the same rule on context_lens and
- * slot_mapping as pa_decode.
+ * Launched as a programmatic dependent, with the same rule on context_lens, block_tables
+ * and slot_mapping as pa_decode.
  */
 int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new,
                    int64_t k_new_stride, int64_t v_new_stride, void* k_cache, void* v_cache,
