@@ -549,6 +549,88 @@ def measure_block_sizes(dev, steps: int, warmup: int):
     return res
 
 
+def measure_prefix_sharing(dev, steps: int, warmup: int):
+    """The prefix-sharing workload (B=512, lengths lognormal(6, 1) clipped to 1..4096,
+    groups of 64 sequences share their first 4 physical blocks, H=16, H_kv=8, D=128) at
+    block sizes 16 and 256: the fused decode step timed one launch at a time after an L2
+    flush (a read of a 512 MB buffer: a write would leave dirty lines whose write-back
+    lands in the timed launch), one launch at a time without the flush (shared blocks may
+    then stay in L2 from the step before), and back to back. GB/s are given twice:
+    'logical' counts every sequence's K/V rows, 'unique' each physical row once."""
+    import torch
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300 import workloads
+    hbm_peak, _, peak_src = measured_peaks()
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)  # 512 MB, read only
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {"peak_gbs": hbm_peak, "peak_source": f"{peak_src} HBM copy GB/s"}
+    for bs in (16, 256):
+        case = workloads.workload(4, block_size=bs, poison=False)
+        tot_ctx, kv_bytes, small_bytes, store_bytes = workload_summary(case)
+        Hk, D = case.num_kv_heads, case.head_dim
+        rows = {}  # physical block -> rows read from it (the longest reader's share)
+        for b in range(case.num_seqs):
+            n = int(case.context_lens[b])
+            for j in range(-(-n // bs)):
+                blk = int(case.block_tables[b, j])
+                rows[blk] = max(rows.get(blk, 0), min(bs, n - j * bs))
+        uniq_bytes = sum(rows.values()) * Hk * D * 2 * 2
+        kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+        q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+        slots = torch.from_numpy(case.slot_mapping).to(dev)
+        bt = torch.from_numpy(case.block_tables).to(dev)
+        ctx = torch.from_numpy(case.context_lens).to(dev)
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = pk.DecodeWorkspace(case.num_seqs, case.num_heads, Hk, D, device=dev)
+
+        def step():
+            pk.pa_decode_step(out, q, kn, vn, kc, vc, slots, bt, ctx, workspace=ws, dev_err=err,
+                              stream=stream)
+
+        def flush_l2():
+            torch.amax(flush, dim=0, keepdim=True, out=sink)
+
+        for _ in range(max(warmup, 3)):
+            flush_l2()
+            step()
+        torch.cuda.synchronize(dev)
+        times = {}
+        for mode in ("flushed", "warm"):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            for a, b in ev:
+                if mode == "flushed":
+                    flush_l2()
+                a.record(stream)
+                step()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            times[mode] = statistics.median(a.elapsed_time(b) for a, b in ev)
+        lo, hi = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lo.record(stream)
+        for _ in range(steps):
+            step()
+        hi.record(stream)
+        torch.cuda.synchronize(dev)
+        times["loop"] = lo.elapsed_time(hi) / steps
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item())} at block size {bs}")
+        entry = {"workload": case.name, "num_seqs": case.num_seqs,
+                 "total_context_tokens": tot_ctx, "shared_blocks": case.shared_blocks,
+                 "logical_kv_bytes": kv_bytes, "unique_kv_bytes": uniq_bytes}
+        for mode, ms in times.items():
+            entry[mode] = {"step_us": ms * 1e3,
+                           "logical_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+                           "unique_gbs": uniq_bytes / (ms * 1e-3) / 1e9,
+                           "unique_frac_of_hbm": uniq_bytes / (ms * 1e-3) / 1e9 / hbm_peak}
+        res[f"bs{bs}"] = entry
+        del kc, vc, case
+    del flush
+    return res
+
+
 def measure_sampler(dev, steps: int, warmup: int):
     """Gumbel-max sampling of one token per row: B=256 rows of the Qwen3 vocabulary
     (V=151936), fp32 logits N(0, 9), T ~ U[0.3, 1.5], random seeds and offsets. The
@@ -874,11 +956,19 @@ def run_ours(args):
         line["staged_write"] = measure_staged(dev, steps=min(args.steps, 50), warmup=args.warmup)
         line["sampler"] = measure_sampler(dev, steps=min(args.steps, 50), warmup=args.warmup)
         line["variants"] = measure_variants(dev, steps=min(args.steps, 30), warmup=args.warmup)
+        line["prefix_sharing"] = measure_prefix_sharing(dev, steps=min(args.steps, 30),
+                                                        warmup=args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
-        cb = cpu_baseline(case, seconds=args.cpu_seconds)
+        stored = oracle_store(case)
+        cb = cpu_baseline(case, seconds=args.cpu_seconds, stored=stored)
+        # the same oracle on one host thread, on a shorter sample
+        c1 = cpu_baseline(case, seconds=max(args.cpu_seconds / 3, 1.0), threads=1,
+                          stored=stored)
         line["cpu_baseline"] = {"value": cb["gbs"], "unit": "GB/s", "cores": cb["cores"],
                                 "kind": "oracle", "sample": cb["sample"],
-                                "seqs_per_s": cb["seqs_per_s"]}
+                                "seqs_per_s": cb["seqs_per_s"],
+                                "single_thread": {"value": c1["gbs"], "unit": "GB/s",
+                                                  "cores": c1["cores"], "sample": c1["sample"]}}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -907,6 +997,8 @@ def main():
                     help="with --variants-only: time this variant alone")
     ap.add_argument("--sampler-only", action="store_true",
                     help="time only the Gumbel-max sampler (for profiler captures)")
+    ap.add_argument("--prefix-only", action="store_true",
+                    help="time only the prefix-sharing decode step at block sizes 16 and 256")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="override the block pool size (a smaller pool for profiler captures)")
     args = ap.parse_args()
@@ -927,6 +1019,13 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps(measure_sampler(dev, args.steps, args.warmup)))
+    elif args.prefix_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_prefix_sharing(dev, args.steps, args.warmup)))
     elif args.prefill_only:
         import torch
         import paged_kv_cache_107_gb300 as pk

@@ -172,9 +172,11 @@ static int attend_row(double* o, double* lse, const double* qv, const uint16_t* 
   return ORC_OK;
 }
 
+/* nthreads > 0: that many threads; 0: every host core (so a one-thread call before does
+ * not leave later calls on one thread). */
 static int set_threads(int nthreads) {
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  omp_set_num_threads(nthreads > 0 ? nthreads : omp_get_num_procs());
   return omp_get_max_threads();
 #else
   (void)nthreads;
