@@ -83,3 +83,79 @@ def test_decode_step_graph_replay_with_padding_rows(fused):
         got = to_f64(out)
         assert_close(got[:real], ref, f"replay with {real} real rows")
         assert np.all(got[real:] == 0.0), "padding rows must be zero"
+
+
+def test_prefill_step_graph_replay_with_padding_sequences():
+    """Store + chunked prefill captured once for a bucket (4 sequences, 1024 new-token rows,
+    at most 512 new tokens per sequence) and replayed on fresh batches over the same static
+    buffers: unused sequences have no tokens (cu_seqlens repeat), unused token rows have
+    slot -1. Every real output row must match the oracle; the tensor maps built at capture
+    time stay valid because the cache buffers do not move."""
+    dev = torch.device("cuda")
+    S, N, maxq, maxk, H, Hk, D, bs = 4, 1024, 512, 2048, 16, 8, 128, 256
+    maxb = maxk // bs
+    nb = 64
+    kc = torch.zeros((nb, bs, Hk, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    q = torch.zeros((N, H, D), dtype=torch.bfloat16, device=dev)
+    k_new = torch.zeros((N, Hk, D), dtype=torch.bfloat16, device=dev)
+    v_new = torch.zeros_like(k_new)
+    slots = torch.full((N,), -1, dtype=torch.int32, device=dev)
+    bt = torch.full((S, maxb), -1, dtype=torch.int32, device=dev)
+    cu_q = torch.zeros((S + 1,), dtype=torch.int32, device=dev)
+    cu_k = torch.zeros((S + 1,), dtype=torch.int32, device=dev)
+    out = torch.zeros((N, H, D), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        pk.pa_store_kvcache(k_new, v_new, kc, vc, slots, dev_err=err)
+        pk.pa_prefill_varlen(out, q, kc, vc, bt, cu_q, cu_k, maxq, maxk, causal=True,
+                             dev_err=err)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture (no sequences yet)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+
+    rng = np.random.default_rng(107902)
+    for real in (4, 2, 1):
+        new = rng.integers(1, maxq // 2 + 1, size=real)
+        cached = rng.integers(0, maxk - maxq + 1, size=real)
+        case = workloads.prefill_case(cached, new, H, Hk, D, bs, num_blocks=nb,
+                                      seed=int(rng.integers(1 << 30)))
+        T = int(case.cu_seqlens_q[-1])
+        assert T <= N
+        kc.copy_(case.k_cache.to(dev))
+        vc.copy_(case.v_cache.to(dev))
+        q.zero_()
+        q[:T] = case.q.to(dev)
+        k_new[:T] = case.k_new.to(dev)
+        v_new[:T] = case.v_new.to(dev)
+        slots.fill_(-1)
+        slots[:T] = torch.from_numpy(case.slot_mapping).to(dev)
+        bt.fill_(-1)
+        bt[:real, :case.block_tables.shape[1]] = torch.from_numpy(case.block_tables).to(dev)
+        cq = np.full(S + 1, T, np.int32)
+        ck = np.full(S + 1, int(case.cu_seqlens_k[-1]), np.int32)
+        cq[:real + 1] = case.cu_seqlens_q
+        ck[:real + 1] = case.cu_seqlens_k
+        cu_q.copy_(torch.from_numpy(cq))
+        cu_k.copy_(torch.from_numpy(ck))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+        ok, ov = oracle.store_kvcache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                      case.slot_mapping)
+        assert np.array_equal(bits(kc), ok) and np.array_equal(bits(vc), ov)
+        ref = oracle.prefill(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+                             case.cu_seqlens_q, case.cu_seqlens_k, causal=True)
+        got = to_f64(out)
+        assert np.all(np.isfinite(got[:T]))
+        assert_close(got[:T], ref, f"prefill replay with {real} sequences")
+        assert np.all(np.isnan(got[T:])), "rows past the batch's tokens must not be written"
