@@ -114,6 +114,80 @@ def test_split_counts_agree_closely():
         assert np.max(np.abs(o - outs[0])) <= 2 * 2.0 ** -8 * (np.abs(outs[0]).max() + 1e-3)
 
 
+def _ordered_bf16(t):
+    """bf16 bit patterns as integers in the order of the values they encode (+0 and -0
+    both map to 0), so that adjacent representable values differ by one."""
+    b = bits(t).astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+SPLIT_GRIDS = (1, 0, 300, 601)  # one CTA (no split), automatic, many CTAs
+
+
+def _split_outputs(H, Hk, D, seed):
+    lens = list(np.random.default_rng(seed).integers(1, 6000, 24)) + [1, 256, 257]
+    case = workloads.decode_case(lens, H, Hk, D, 256, seed=seed, num_blocks=1024)
+    dc = DeviceCase(case)
+    dc.store()
+    outs = [dc.decode(grid_ctas=g) for g in SPLIT_GRIDS]
+    assert dc.dev_err() == 0
+    return case, outs
+
+
+@pytest.mark.parametrize("H,Hk", [(16, 8), (8, 8), (4, 2)])
+def test_split_counts_round_to_adjacent_bf16(H, Hk):
+    """CUDA-core kernel (1 or 2 query heads per KV head, probabilities kept in fp32): the
+    split-softmax identity is exact, so the split count only changes fp32 rounding (about
+    1e-6 relative), far below one bf16 step (2^-8 relative). The bf16 outputs of one CTA,
+    the automatic grid and many CTAs are therefore, element by element, the same value or
+    adjacent representable values. Near zero the bf16 step is finer than that rounding, so
+    two values closer than 1e-5 of their row's largest magnitude also pass."""
+    case, outs = _split_outputs(H, Hk, 128, 607 + H + Hk)
+    base = _ordered_bf16(outs[0])
+    ref = to_f64(outs[0])
+    row_max = np.abs(ref).max(axis=-1, keepdims=True)
+    for g, o in zip(SPLIT_GRIDS[1:], outs[1:]):
+        steps = np.abs(_ordered_bf16(o) - base)
+        tiny = np.abs(to_f64(o) - ref) <= 1e-5 * row_max
+        bad = (steps > 1) & ~tiny
+        assert not bad.any(), (f"grid {g}: {int(bad.sum())} elements more than one bf16 step "
+                               f"from the one-CTA result; worst {int(steps.max())}")
+
+
+def _bf16_step(x):
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    _, e = np.frexp(np.maximum(np.abs(x), 2.0 ** -126))
+    return np.ldexp(1.0, e - 8)
+
+
+@pytest.mark.parametrize("H,Hk,D", [(32, 8, 128), (64, 8, 128), (16, 8, 64)])
+def test_split_counts_tensor_core_within_p_rounding(H, Hk, D):
+    """Tensor-core kernel: each probability p_t = 2^(s_t - m) is rounded to bf16 (relative
+    error <= 2^-9) before the P V product, and the offset m is the running maximum of the
+    keys seen so far, which depends on where the splits fall. Two split counts therefore
+    differ by at most 2 * 2^-9 * (sum_t p_t |v_t|) / (sum_t p_t) per element, plus one bf16
+    step of output rounding and fp32 rounding. The weighted mean of |v| comes from the
+    oracle run on |V|."""
+    case, outs = _split_outputs(H, Hk, D, 611 + H + D)
+    ok, ov = oracle_after_store(case)
+    abs_v = from_bits(ov).abs()
+    mean_abs_v = oracle.decode(case.q, from_bits(ok), abs_v, case.block_tables,
+                               case.context_lens)
+    ref = to_f64(outs[0])
+    row_max = np.abs(ref).max(axis=-1, keepdims=True)
+    for g, o in zip(SPLIT_GRIDS[1:], outs[1:]):
+        got = to_f64(o)
+        bound = (2.0 ** -8 * mean_abs_v + _bf16_step(np.maximum(np.abs(got), np.abs(ref)))
+                 + 1e-5 * row_max)
+        diff = np.abs(got - ref)
+        bad = diff > bound
+        assert not bad.any(), (f"grid {g}: {int(bad.sum())} elements beyond the rounding bound; "
+                               f"worst ratio {float((diff / bound).max()):.3f}")
+        # the bound is a worst case; the typical difference sits far below it
+        assert float(np.median(diff / bound)) < 0.25
+
+
 def test_sharp_softmax_cases():
     """Near one-hot attention (one key aligned with q, scaled up) and constant values:
     cases where the output is far from the near-uniform average of N(0,1) data."""
