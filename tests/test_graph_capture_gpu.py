@@ -159,3 +159,78 @@ def test_prefill_step_graph_replay_with_padding_sequences():
         assert np.all(np.isfinite(got[:T]))
         assert_close(got[:T], ref, f"prefill replay with {real} sequences")
         assert np.all(np.isnan(got[T:])), "rows past the batch's tokens must not be written"
+
+
+def test_decode_step_graphs_per_batch_bucket():
+    """One graph per batch-size bucket (1, 2, 4, 8, 16, 32), as the engine captures them
+    ("3.6 ModelRunner、CUDA Graph 与性能基准", section 5), all over slices of one set of
+    static buffers and one workspace sized for the largest bucket. Each fresh batch replays
+    the smallest bucket that holds it, its extra rows padding; the outputs must match the
+    oracle."""
+    dev = torch.device("cuda")
+    buckets = (1, 2, 4, 8, 16, 32)
+    top, H, Hk, D, bs = buckets[-1], 16, 8, 128, 32
+    maxb, nb = 24, 1024
+    kc = torch.zeros((nb, bs, Hk, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    q = torch.zeros((top, H, D), dtype=torch.bfloat16, device=dev)
+    k_new = torch.zeros((top, Hk, D), dtype=torch.bfloat16, device=dev)
+    v_new = torch.zeros_like(k_new)
+    slots = torch.full((top,), -1, dtype=torch.int32, device=dev)
+    ctx = torch.zeros((top,), dtype=torch.int32, device=dev)
+    bt = torch.full((top, maxb), -1, dtype=torch.int32, device=dev)
+    out = torch.zeros((top, H, D), dtype=torch.bfloat16, device=dev)
+    ws = pk.DecodeWorkspace(top, H, Hk, D, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(n):
+        pk.pa_decode_step(out[:n], q[:n], k_new[:n], v_new[:n], kc, vc, slots[:n], bt[:n],
+                          ctx[:n], workspace=ws, dev_err=err)
+
+    graphs = {}
+    pool = None
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for n in buckets:
+            step(n)  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for n in reversed(buckets):  # largest first, sharing one memory pool
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, pool=pool):
+            step(n)
+        pool = g.pool()
+        graphs[n] = g
+
+    rng = np.random.default_rng(107903)
+    for real in (1, 3, 7, 12, 32, 20, 2):
+        n = min(b for b in buckets if b >= real)
+        lens = rng.integers(1, maxb * bs, size=real)
+        case = workloads.decode_case(lens, H, Hk, D, bs, num_blocks=nb,
+                                     seed=int(rng.integers(1 << 30)), max_blocks=maxb)
+        kc.copy_(case.k_cache.to(dev))
+        vc.copy_(case.v_cache.to(dev))
+        q.zero_()
+        q[:real] = case.q.to(dev)
+        k_new[:real] = case.k_new.to(dev)
+        v_new[:real] = case.v_new.to(dev)
+        slots.fill_(-1)
+        slots[:real] = torch.from_numpy(case.slot_mapping).to(dev)
+        ctx.zero_()
+        ctx[:real] = torch.from_numpy(case.context_lens).to(dev)
+        bt.fill_(-1)
+        bt[:real] = torch.from_numpy(case.block_tables).to(dev)
+        out.fill_(float("nan"))
+        graphs[n].replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+        ok, ov = oracle.store_kvcache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                      case.slot_mapping)
+        assert np.array_equal(bits(kc), ok) and np.array_equal(bits(vc), ov)
+        ref = oracle.decode(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+                            case.context_lens)
+        got = to_f64(out)
+        assert_close(got[:real], ref, f"{real} sequences in the bucket of {n}")
+        assert np.all(got[real:n] == 0.0), "padding rows of the bucket must be zero"
+        assert np.all(np.isnan(got[n:])), "rows past the bucket must not be written"
