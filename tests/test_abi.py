@@ -104,6 +104,14 @@ def test_validation_without_launch(lib):
     rc = lib.pa_prefill_varlen(vp, vp, vp, vp, vp, 2, vp, vp, 1, 10, 600, 16, 8, 128, 1, 256,
                                ctypes.c_int64(4), 1, ctypes.c_float(0), None, None)
     assert rc in (2, 3)
+    # empty batches are successful no-ops that touch neither the pointers nor CUDA
+    rc = lib.pa_decode(None, None, None, None, None, 0, None, 0, 16, 8, 128, 1, 16,
+                       ctypes.c_int64(4), ctypes.c_float(0), 0, None, ctypes.c_size_t(0), None,
+                       None)
+    assert rc == 0
+    rc = lib.pa_prefill_varlen(None, None, None, None, None, 0, None, None, 0, 0, 0, 16, 8, 128,
+                               1, 256, ctypes.c_int64(4), 1, ctypes.c_float(0), None, None)
+    assert rc == 0
 
 
 def test_header_is_plain_c_and_links(lib, tmp_path):
