@@ -404,8 +404,8 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
     """head_dim 64 / IEEE fp16 variants on the shapes of the decode step (workload 2: the
     fused store + decode, one launch) and of the chunked prefill (workload 5); and the
     decode step with 4 and 8 query heads per KV head (the tensor-core path). `only` keeps
-    one variant (its tag); `pool_blocks` sizes the 4- and 8-group block pools (at least
-    the 2048 blocks their tables use) for profiler captures."""
+    one variant (its tag); `pool_blocks` sizes the decode steps' block pools (at least the
+    1229 blocks their tables use) for profiler captures."""
     import torch
     import paged_kv_cache_107_gb300 as pk
     from paged_kv_cache_107_gb300 import workloads
@@ -417,7 +417,8 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
         if only is not None and tag != only:
             continue
         if heads == 16:
-            case = workloads.workload(2, poison=True, head_dim=D, dtype=dt)
+            case = workloads.workload(2, poison=True, num_blocks=pool_blocks, head_dim=D,
+                                      dtype=dt)
         else:  # the same lengths and tables with 4 or 8 query heads per KV head
             base = workloads.workload(2, poison=False)
             case = workloads.decode_case(base.context_lens, heads, 8, D, 256,
@@ -470,9 +471,9 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
             "alg_bytes_per_launch": alg,
             "loop_step_us": loop_ms * 1e3,
             "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9}
-        if tag == "g8":
-            res["decode_step_" + tag]["traffic"] = kernel_traffic(DECODE_TC_SOURCES,
-                                                                  "decode_tc_g8_w2_b256.md")
+        summary = {"g8": "decode_tc_g8_w2_b256.md", "d64_bf16": "decode_tc_d64_w2_b256.md"}
+        if tag in summary:
+            res["decode_step_" + tag]["traffic"] = kernel_traffic(DECODE_TC_SOURCES, summary[tag])
         del kc, vc, case
         if heads == 16 and only is None:
             res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
