@@ -30,8 +30,9 @@
 //    head and the tile lies in one block), else one per token row. Tiles never need block
 //    alignment: each token's row can be addressed through the block table on its own.
 //  * Launched as a programmatic dependent of the previous kernel on the stream: the
-//    prologue reads only context_lens, the producer prefetches its first tiles' K/V runs
-//    into L2, and everything that reads q, the new rows or the caches, or writes the
+//    prologue reads context_lens (and, in the fused step, slot_mapping for its checks),
+//    the producer reads the block-table rows of its first tiles to prefetch their K/V
+//    runs into L2, and everything that reads q, the new rows or the caches, or writes the
 //    output or the workspace, waits for the previous grid first.
 //  * The last CTA of a split sequence combines the partials in CTA order
 //    (combine_partials): the LSEs of every head and segment in one round trip per batch,
@@ -45,6 +46,7 @@
 //    pre-scaled q; fp32 accumulation; one bf16 rounding at the end.
 #pragma once
 
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -1027,14 +1029,14 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 template <int HS, int G, bool FUSED, int D, bool F16>
 int launch_decode_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
   using C = DecCfg<HS, G, D>;
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   const int dev = info.device;
   if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(paged_decode_kernel<HS, G, FUSED, D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM) != cudaSuccess)
       return PA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   const int slabs = a.num_kv_heads / HS;
   dim3 grid((unsigned)a.grid_ctas, (unsigned)slabs);

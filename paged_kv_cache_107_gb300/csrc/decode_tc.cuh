@@ -33,6 +33,7 @@
 //    meets a zero probability.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <string.h>
 
@@ -779,14 +780,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HS, bool FUSED, int D, bool F16>
 int launch_decode_tc_t(const DecodeArgs& a, const DeviceInfo& info, cudaStream_t stream) {
   using TC = TcCfg<HS, D>;
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   const int dev = info.device;
   if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(paged_decode_tc_kernel<HS, FUSED, D, F16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC::SMEM) != cudaSuccess)
       return PA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   // tokens per TMA box: the largest power of two dividing block_size, at most a stage's
   // tokens; below 8 the stage is filled by 16-byte cp.async copies instead

@@ -37,13 +37,12 @@
 //    the end of its protocol and frees its tensor memory.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
@@ -448,13 +447,13 @@ int launch_prefill_t(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t 
   constexpr int P = kRows / G;
   const size_t smem = sizeof(PrefillSmem<D>) + 1024;
   static_assert(sizeof(PrefillSmem<D>) + 1024 <= 227 * 1024, "shared memory budget");
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   if (info.device < 0 || info.device >= 64) return PA_ERR_CUDA;
-  if (!attr_done[info.device]) {
+  if (!attr_done[info.device].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(paged_prefill_kernel<G, D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return PA_ERR_CUDA;
-    attr_done[info.device] = true;
+    attr_done[info.device].store(true, std::memory_order_release);
   }
   const int q_tiles = (a.max_seqlen_q + 2 * P - 1) / (2 * P);  // pairs of query tiles
   if (q_tiles > 65535) return PA_ERR_UNSUPPORTED;

@@ -26,6 +26,7 @@
 //    then one thread), does one atomicMax into the row's key and adds its tile count to the
 //    row's arrival counter; the CTA that completes the count writes the index and resets
 //    key and counter to zero for the next call. One launch, deterministic.
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -438,14 +439,14 @@ namespace {
 template <typename T, int CW>
 int launch_ring(const SampleArgs& a, cudaStream_t stream, int num_sms) {
   const size_t smem = (size_t)kRingStages * kTileBytes + sizeof(RingCtrl) + 128;
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];  // zero-initialised: false
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(gumbel_sample_ring_kernel<T, CW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return PA_ERR_CUDA;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   const int64_t nt = (int64_t)a.num_rows * a.chunks;
   const int grid = (int)(nt < num_sms ? nt : num_sms);
