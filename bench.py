@@ -61,6 +61,7 @@ def source_sha256(*names) -> str:
 DECODE_SOURCES = ("decode_kernel.cuh", "pa_device.cuh")
 DECODE_TC_SOURCES = ("decode_tc.cuh", "decode_kernel.cuh", "pa_device.cuh")
 PREFILL_SOURCES = ("prefill_kernel.cuh", "prefill.cu", "umma.cuh", "pa_device.cuh")
+STORE_SOURCES = ("store.cu", "pa_device.cuh")
 
 
 def profile_value(sources, summary: str, key: str):
@@ -391,6 +392,14 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128
            "peak_tflops": tflops_peak, "peak_source": f"{src} bf16 dense (sustained)",
            "tokens_per_s": nq / (pf_ms * 1e-3),
            "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
+    if head_dim == 128 and (dtype is None or dtype == torch.bfloat16):
+        hbm_peak, _, hsrc = measured_peaks()
+        # the store of the chunk's new tokens: K and V rows read and written once
+        res["store_roofline"] = {
+            "kernel": "store_kvcache_kernel", "bound": "hbm", "unit": "GB/s",
+            "achieved": res["store_gbs"], "peak": hbm_peak, "frac": res["store_gbs"] / hbm_peak,
+            "peak_source": f"{hsrc} HBM copy GB/s", "alg_bytes_per_launch": store_bytes,
+            "traffic": kernel_traffic(STORE_SOURCES, "store_kvcache_w5_prefill.md")}
     if head_dim == 128 and (dtype is None or dtype == torch.bfloat16):
         res["roofline"] = {
             "kernel": "paged_prefill_kernel", "bound": "tensor", "unit": "TFLOP/s",
@@ -998,6 +1007,8 @@ def main():
                     help="with --variants-only: time this variant alone")
     ap.add_argument("--sampler-only", action="store_true",
                     help="time only the Gumbel-max sampler (for profiler captures)")
+    ap.add_argument("--staged-only", action="store_true",
+                    help="time only the staged block-table writes (for profiler captures)")
     ap.add_argument("--prefix-only", action="store_true",
                     help="time only the prefix-sharing decode step at block sizes 16 and 256")
     ap.add_argument("--pool-blocks", type=int, default=None,
@@ -1020,6 +1031,13 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps(measure_sampler(dev, args.steps, args.warmup)))
+    elif args.staged_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_staged(dev, args.steps, args.warmup)))
     elif args.prefix_only:
         import torch
         import paged_kv_cache_107_gb300 as pk
