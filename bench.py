@@ -489,6 +489,7 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
                                                     head_dim=D, dtype=dt)
     if only is None:
         res["decode_step_block_sizes"] = measure_block_sizes(dev, min(steps, 30), warmup)
+        res["decode_step_batch_sizes"] = measure_batch_sizes(dev, min(steps, 30), warmup)
     return res
 
 
@@ -638,6 +639,69 @@ def measure_prefix_sharing(dev, steps: int, warmup: int):
         res[f"bs{bs}"] = entry
         del kc, vc, case
     del flush
+    return res
+
+
+def measure_batch_sizes(dev, steps: int, warmup: int):
+    """The fused decode step on the first B sequences of the decode-step workload (ctx
+    U{100..2048}, H=16, H_kv=8, D=128, bs=256) for B = 1 .. 256: one launch at a time and
+    back to back. A least-squares line through (K/V bytes, time) for B >= 16 separates the
+    streaming rate from the fixed cost of a launch, which sets the latency of small
+    batches."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300 import workloads
+    full = workloads.workload(2, poison=False)
+    kc, vc = full.k_cache.to(dev), full.v_cache.to(dev)
+    H, Hk, D = full.num_heads, full.num_kv_heads, full.head_dim
+    stream = torch.cuda.current_stream(dev)
+    res, pts, pts_loop = {}, [], []
+    for B in (1, 4, 16, 64, 128, 256):
+        q = full.q[:B].to(dev)
+        kn, vn = full.k_new[:B].to(dev), full.v_new[:B].to(dev)
+        slots = torch.from_numpy(full.slot_mapping[:B].copy()).to(dev)
+        bt = torch.from_numpy(full.block_tables[:B].copy()).to(dev)
+        ctx = torch.from_numpy(full.context_lens[:B].copy()).to(dev)
+        out = torch.empty_like(q)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = pk.DecodeWorkspace(B, H, Hk, D, device=dev)
+
+        def step():
+            pk.pa_decode_step(out, q, kn, vn, kc, vc, slots, bt, ctx, workspace=ws, dev_err=err,
+                              stream=stream)
+
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        lo, hi = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lo.record(stream)
+        for _ in range(steps):
+            step()
+        hi.record(stream)
+        torch.cuda.synchronize(dev)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item())} at batch {B}")
+        kv = int(full.context_lens[:B].astype(np.int64).sum()) * Hk * D * 2 * 2
+        per = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+        loop = lo.elapsed_time(hi) / steps * 1e3
+        res[f"b{B}"] = {"kv_bytes": kv, "step_us": per, "loop_step_us": loop,
+                        "kv_gbs": kv / per / 1e3, "loop_kv_gbs": kv / loop / 1e3}
+        if B >= 16:
+            pts.append((kv, per))
+            pts_loop.append((kv, loop))
+    for name, p in (("fit_per_launch", pts), ("fit_back_to_back", pts_loop)):
+        x = np.array([a for a, _ in p], np.float64)
+        y = np.array([b for _, b in p], np.float64)
+        slope, icpt = np.polyfit(x, y, 1)  # us per byte, us
+        res[name] = {"stream_gbs": 1e-3 / slope, "fixed_us": icpt}
+    del kc, vc
     return res
 
 
@@ -1009,6 +1073,8 @@ def main():
                     help="time only the Gumbel-max sampler (for profiler captures)")
     ap.add_argument("--staged-only", action="store_true",
                     help="time only the staged block-table writes (for profiler captures)")
+    ap.add_argument("--batches-only", action="store_true",
+                    help="time only the decode step at batch sizes 1..256")
     ap.add_argument("--prefix-only", action="store_true",
                     help="time only the prefix-sharing decode step at block sizes 16 and 256")
     ap.add_argument("--pool-blocks", type=int, default=None,
@@ -1038,6 +1104,13 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps(measure_staged(dev, args.steps, args.warmup)))
+    elif args.batches_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_batch_sizes(dev, args.steps, args.warmup)))
     elif args.prefix_only:
         import torch
         import paged_kv_cache_107_gb300 as pk

@@ -249,15 +249,20 @@ __device__ __forceinline__ LaneVec<DPL> zero_lane() {
 // c_lo.. that processed parts of sequence b, in CTA order, for the G query heads of the
 // group, and write the G output rows. One warp. Lane h + G*j holds the LSE of head h in
 // segment j of a batch of 32/G segments, so the LSEs of every head arrive in one round
-// trip per batch and the per-head maxima come from shuffles; then, segment by segment, the
-// partial outputs of up to four heads are loaded together (one round trip per segment
-// and group of four heads, not one per segment and head). GMAX bounds G.
+// trip per batch and the per-head maxima come from shuffles; then the partial outputs of
+// up to four heads and of SU consecutive segments are loaded together before any of them
+// is accumulated (one round trip per SU segments and group of four heads; the sums still
+// run in CTA order, so the result does not depend on SU). GMAX bounds G.
 template <int D, bool F16, int GMAX>
 __device__ __forceinline__ void combine_partials(const DecodeArgs& a, int b, int kvh, int G,
                                                  int64_t c_lo, int nseg, int64_t NT, int g_eff,
                                                  int64_t pb, int lane) {
   constexpr int CPL = D / 32;                 // combined dims per lane
   constexpr int HG = GMAX < 4 ? GMAX : 4;     // heads combined together
+  // segments whose loads are in flight together, within the registers the kernel has
+  // left: four for groups of 1-2 heads (the CUDA-core kernel), two for four heads of 64
+  // dims, one for four heads of 128 dims (the tensor-core kernel)
+  constexpr int SU = HG <= 2 ? 4 : (HG * CPL <= 8 ? 2 : 1);
   const int H = a.num_heads;
   const int SB = 32 / G;                      // segments per batch
   const int my_h = lane % G, my_j = lane / G;
@@ -295,41 +300,50 @@ __device__ __forceinline__ void combine_partials(const DecodeArgs& a, int b, int
           m_h[q] = nm;
         }
       }
-      for (int j = 0; j < nb; ++j) {
-        const int64_t cj = c_lo + s0 + j;
-        const int slj = __shfl_sync(0xffffffffu, sl, G * j);
-        float w[HG];
-        float po[HG][CPL];
+      for (int j0 = 0; j0 < nb; j0 += SU) {
+        float w[SU][HG];
+        float po[SU][HG][CPL];
 #pragma unroll
-        for (int q = 0; q < HG; ++q) {
-          w[q] = 0.f;
+        for (int u = 0; u < SU; ++u) {
+          const int j = j0 + u;
+          const bool seg = j < nb;
+          const int64_t cj = c_lo + s0 + j;
+          const int slj = __shfl_sync(0xffffffffu, sl, seg ? G * j : 0);
 #pragma unroll
-          for (int e = 0; e < CPL; ++e) po[q][e] = 0.f;
-          if (h0 + q < G) {
-            const float l = __shfl_sync(0xffffffffu, ls, h0 + q + G * j);
-            w[q] = (m_h[q] == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2(l - m_h[q]);
-            if (w[q] != 0.f) {
-              const float* src =
-                  a.part_o + ((cj * 2 + slj) * H + kvh * G + h0 + q) * D + lane * CPL;
-              if constexpr (CPL == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-                po[q][0] = v.x;
-                po[q][1] = v.y;
-                po[q][2] = v.z;
-                po[q][3] = v.w;
-              } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-                po[q][0] = v.x;
-                po[q][1] = v.y;
+          for (int q = 0; q < HG; ++q) {
+            w[u][q] = 0.f;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) po[u][q][e] = 0.f;
+            const float l = __shfl_sync(0xffffffffu, ls, seg ? h0 + q + G * j : 0);
+            if (seg && h0 + q < G) {
+              w[u][q] = (m_h[q] == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2(l - m_h[q]);
+              if (w[u][q] != 0.f) {
+                const float* src =
+                    a.part_o + ((cj * 2 + slj) * H + kvh * G + h0 + q) * D + lane * CPL;
+                if constexpr (CPL == 4) {
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                  po[u][q][0] = v.x;
+                  po[u][q][1] = v.y;
+                  po[u][q][2] = v.z;
+                  po[u][q][3] = v.w;
+                } else {
+                  const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                  po[u][q][0] = v.x;
+                  po[u][q][1] = v.y;
+                }
               }
             }
           }
         }
+        // accumulate in segment (CTA) order
 #pragma unroll
-        for (int q = 0; q < HG; ++q) {
-          den[q] += w[q];
+        for (int u = 0; u < SU; ++u) {
 #pragma unroll
-          for (int e = 0; e < CPL; ++e) acc[q][e] = fmaf(w[q], po[q][e], acc[q][e]);
+          for (int q = 0; q < HG; ++q) {
+            den[q] += w[u][q];
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) acc[q][e] = fmaf(w[u][q], po[u][q][e], acc[q][e]);
+          }
         }
       }
     }
@@ -413,7 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t nt = 0;
     for (int w = 0; w < kThreads / 32; ++w) nt += ctl.red[w];
     ctl.nt = nt;
-    const int g_eff = (int)(nt < (int64_t)gridDim.x ? nt : (int64_t)gridDim.x);
+    // CTAs that own tiles: every CTA of the grid, unless the stream is too short to give
+    // each at least min_tiles
+    const int64_t mt = a.min_tiles > 1 ? a.min_tiles : 1;
+    const int64_t want = (nt + mt - 1) / mt;
+    const int g_eff = (int)(want < (int64_t)gridDim.x ? want : (int64_t)gridDim.x);
     ctl.g_eff = g_eff;
     if (c < g_eff) {
       ctl.x0 = tile_begin(c, nt, g_eff);

@@ -69,7 +69,8 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
     return PA_ERR_ALIGN;
   pa::DeviceInfo info;
   if (!pa::current_device_info(&info)) return PA_ERR_CUDA;
-  if (grid_ctas == 0) grid_ctas = info.num_sms;
+  const bool auto_grid = grid_ctas == 0;
+  if (auto_grid) grid_ctas = info.num_sms;
   if (grid_ctas > pa::decode_max_ctas(info)) return PA_ERR_SHAPE;
   // the partial-result slots are indexed by CTA, so size them for this grid only
   size_t off_c, off_l, off_o, total;
@@ -100,6 +101,7 @@ extern "C" int pa_decode_noalloc(void* out, const void* q, const void* k_cache,
   if (!(s > 0.f) || isnan(s)) s = 1.0f / sqrtf((float)head_dim);
   a.scale_log2 = s * 1.4426950408889634f;
   a.grid_ctas = grid_ctas;
+  a.min_tiles = auto_grid ? pa::kDecodeMinTilesPerCta : 1;
   a.counters = reinterpret_cast<int*>(ws + off_c);
   a.part_lse = reinterpret_cast<float*>(ws + off_l);
   a.part_o = reinterpret_cast<float*>(ws + off_o);

@@ -216,7 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t nt = 0;
     for (int w = 0; w < kThreads / 32; ++w) nt += ctl.red[w];
     ctl.nt = nt;
-    const int g_eff = (int)(nt < (int64_t)gridDim.x ? nt : (int64_t)gridDim.x);
+    // CTAs that own tiles: every CTA of the grid, unless the stream is too short to give
+    // each at least min_tiles
+    const int64_t mt = a.min_tiles > 1 ? a.min_tiles : 1;
+    const int64_t want = (nt + mt - 1) / mt;
+    const int g_eff = (int)(want < (int64_t)gridDim.x ? want : (int64_t)gridDim.x);
     ctl.g_eff = g_eff;
     if (c < g_eff) {
       ctl.x0 = tile_begin(c, nt, g_eff);

@@ -212,7 +212,8 @@ static int decode_entry(void* out, const void* q, const void* k_cache, const voi
   DeviceInfo info;
   if (!current_device_info(&info)) return PA_ERR_CUDA;
   const int max_ctas = decode_max_ctas(info);
-  if (grid_ctas == 0) grid_ctas = info.num_sms;
+  const bool auto_grid = grid_ctas == 0;
+  if (auto_grid) grid_ctas = info.num_sms;
   if (grid_ctas > max_ctas) return PA_ERR_SHAPE;
   size_t off_c, off_l, off_o, total;
   decode_workspace_layout(num_seqs, num_heads, num_kv_heads, max_ctas, &off_c, &off_l, &off_o,
@@ -237,6 +238,7 @@ static int decode_entry(void* out, const void* q, const void* k_cache, const voi
   a.head_dim = head_dim;
   a.f16 = dtype == PA_DTYPE_F16;
   a.grid_ctas = grid_ctas;
+  a.min_tiles = auto_grid ? pa::kDecodeMinTilesPerCta : 1;
   a.counters = reinterpret_cast<int*>(ws + off_c);
   a.part_lse = reinterpret_cast<float*>(ws + off_l);
   a.part_o = reinterpret_cast<float*>(ws + off_o);

@@ -62,6 +62,7 @@ struct DecodeArgs {
   int64_t num_blocks;
   float scale_log2;  // softmax scale * log2(e)
   int grid_ctas;     // CTAs along the key stream (per head slab)
+  int min_tiles;     // fewest key tiles per CTA (1: every CTA of grid_ctas may take work)
   int head_dim;      // 64 or 128
   int f16;           // element type of q, caches, out: 0 = bf16, 1 = IEEE fp16
   int* counters;     // [num_seqs * num_kv_heads]
@@ -75,6 +76,11 @@ struct DecodeArgs {
   float* part_lse;   // [max_ctas * 2 * num_heads]
   int* dev_err;
 };
+
+// With the automatic grid, a CTA takes at least this many key tiles (64 KB of K and V
+// each at H_kv = 8): a short stream is then cut into fewer, longer CTA ranges, so that a
+// small batch's sequences are split into fewer segments to combine.
+constexpr int kDecodeMinTilesPerCta = 4;
 
 // Maximum CTAs along the key stream that a decode workspace is sized for.
 int decode_max_ctas(const DeviceInfo& info);
