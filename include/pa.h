@@ -236,8 +236,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *                   >= ceil(context_lens[b]/block_size) are never read.
  *   context_lens    device, int32 [num_seqs]; 0 writes a zero row and reads nothing.
  *   scale           softmax scale; <= 0 or NaN means 1/sqrt(head_dim).
- *   grid_ctas       number of CTAs that split the key stream (0 = one per SM). The result
- *                   does not depend on it beyond fp32 rounding of the final combine.
+ *   grid_ctas       number of CTAs that split the key stream (0 = automatic: one per SM,
+ *                   but never fewer than four key tiles per CTA, so a short stream is cut
+ *                   into fewer segments). The result does not depend on it beyond the
+ *                   rounding of the final combine.
  *   workspace       device scratch of at least pa_decode_workspace_size(...) bytes,
  *                   256-byte aligned; zero it once when it is created. It holds the
  *                   partial results, then num_seqs*num_kv_heads int32 arrival counters
