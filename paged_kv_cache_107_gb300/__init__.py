@@ -109,6 +109,25 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _one_device(*tensors, stream=None) -> None:
+    """Every tensor lies on one CUDA device, that device is the current one (the library
+    launches there, on its current or the given stream), and a given stream belongs to it.
+    Checked before any launch: a kernel handed another device's pointers would fault."""
+    devs = {t.device for t in tensors if t is not None}
+    if any(d.type != "cuda" for d in devs):
+        raise PagedAttentionError("every tensor must be a CUDA tensor")
+    idx = {torch.cuda.current_device() if d.index is None else d.index for d in devs}
+    if len(idx) > 1:
+        raise PagedAttentionError(f"tensors on several devices: cuda:{sorted(idx)}")
+    cur = torch.cuda.current_device()
+    if idx and idx != {cur}:
+        raise PagedAttentionError(
+            f"tensors are on cuda:{next(iter(idx))} but the current device is cuda:{cur}; "
+            "call under torch.cuda.device(...) of the tensors' device")
+    if stream is not None and stream.device.index is not None and stream.device.index != cur:
+        raise PagedAttentionError(f"stream belongs to {stream.device}, tensors to cuda:{cur}")
+
+
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: Optional[int] = None):
     if not t.is_cuda:
         raise PagedAttentionError(f"{name} must be a CUDA tensor")
@@ -136,6 +155,7 @@ def pa_store_kvcache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
             raise PagedAttentionError(f"{name} rows must be [Hk, D] contiguous")
     if slot_mapping.shape[0] != k.shape[0] or v.shape[0] != k.shape[0]:
         raise PagedAttentionError("slot_mapping / k / v token counts differ")
+    _one_device(k, v, k_cache, v_cache, slot_mapping, dev_err, stream=stream)
     rc = load_library().pa_store_kvcache(
         _ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache), _ptr(v_cache),
         _ptr(slot_mapping), k.shape[0], hk, d, bs, nb, _ptr(dev_err), _stream(stream))
@@ -157,6 +177,7 @@ def pa_staged_write_apply(base: torch.Tensor, rows: torch.Tensor, starts: torch.
     W = rows.shape[0]
     if starts.shape[0] != W or offsets.shape[0] != W + 1:
         raise PagedAttentionError("rows / starts / offsets sizes disagree")
+    _one_device(base, rows, starts, offsets, values, dev_err, stream=stream)
     rc = load_library().pa_staged_write_apply(
         _ptr(base), base.shape[0], base.shape[1], base.stride(0), base.element_size(),
         _ptr(rows), _ptr(starts), _ptr(offsets), _ptr(values), W, values.shape[0],
@@ -226,6 +247,7 @@ def pa_staged_upload_apply(base: torch.Tensor, packed_host: torch.Tensor,
         raise PagedAttentionError("base must be 2-D with contiguous columns")
     if packed_dev.numel() < layout.bytes or packed_host.numel() < layout.bytes:
         raise PagedAttentionError("packed buffers smaller than layout.bytes")
+    _one_device(base, packed_dev, dev_err, stream=stream)
     rc = fn(base.data_ptr(), base.shape[0], base.shape[1], base.stride(0), base.element_size(),
             packed_host.data_ptr(), packed_dev.data_ptr(), ctypes.byref(layout),
             _ptr(dev_err), _stream(stream))
@@ -285,6 +307,8 @@ def pa_gumbel_sample(out: torch.Tensor, logits: torch.Tensor, temperatures: torc
         workspace = _sample_ws.get(key)
         if workspace is None:
             workspace = _sample_ws[key] = SampleWorkspace(B, device=logits.device)
+    _one_device(out, logits, temperatures, seeds, offsets, workspace.buffer, dev_err,
+                stream=stream)
     rc = load_library().pa_gumbel_sample(
         _ptr(out), _ptr(logits), logits.stride(0) if B > 1 else V, PA_DTYPE[logits.dtype], B, V,
         _ptr(temperatures), _ptr(seeds), _ptr(offsets), _ptr(workspace.buffer),
@@ -357,6 +381,8 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
         raise PagedAttentionError("block_tables / context_lens batch mismatch")
     if workspace is None:
         workspace = _default_workspace(B, H, hk, D, q.device)
+    _one_device(out, q, k_cache, v_cache, block_tables, context_lens, workspace.buffer, dev_err,
+                stream=stream)
     rc = load_library().pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(context_lens), B, H, hk, D, PA_DTYPE[q.dtype], bs, nb,
@@ -399,6 +425,8 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
             raise PagedAttentionError(f"{name} must be [B, Hk, D] with contiguous rows")
     if workspace is None:
         workspace = _default_workspace(B, H, hk, D, q.device)
+    _one_device(out, q, k_new, v_new, k_cache, v_cache, slot_mapping, block_tables,
+                context_lens, workspace.buffer, dev_err, stream=stream)
     rc = load_library().pa_decode_step(
         _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0), v_new.stride(0),
         _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(block_tables),
@@ -433,6 +461,8 @@ def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         raise PagedAttentionError("shape mismatch")
     if cu_seqlens_k.shape[0] != S + 1 or block_tables.shape[0] != S:
         raise PagedAttentionError("cu_seqlens / block_tables batch mismatch")
+    _one_device(out, q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, dev_err,
+                stream=stream)
     rc = load_library().pa_prefill_varlen(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), S, int(max_seqlen_q),
@@ -472,6 +502,7 @@ def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         raise PagedAttentionError("shape mismatch")
     if block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise PagedAttentionError("block_tables / context_lens batch mismatch")
+    _one_device(out, q, k_cache, v_cache, block_tables, context_lens, dev_err, stream=stream)
     rc = fn(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
             block_tables.shape[1], _ptr(context_lens), B, H, hk, D, bs, nb,
             float(scale) if scale is not None else 0.0, int(grid_ctas), _ptr(dev_err),
