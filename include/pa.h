@@ -53,7 +53,8 @@ enum pa_status {
   PA_OK = 0,
   PA_ERR_NULL = 1,        /* a required pointer is NULL */
   PA_ERR_SHAPE = 2,       /* inconsistent sizes: H % Hk != 0, block_size <= 0, ... */
-  PA_ERR_UNSUPPORTED = 3, /* head_dim != 128, or a size beyond what the kernels take */
+  PA_ERR_UNSUPPORTED = 3, /* head_dim not 64 or 128, an element type or query-head group
+                             the call does not take, or a size beyond the kernels' limits */
   PA_ERR_WORKSPACE = 4,   /* decode workspace missing or too small */
   PA_ERR_CUDA = 5,        /* a CUDA runtime error (launch, attribute, tensor map) */
   PA_ERR_ALIGN = 6        /* a pointer or stride breaks the 16-byte alignment rule */
