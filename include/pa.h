@@ -86,19 +86,22 @@ int pa_version(void);
  * token's K/V at its slot); "3.6 ModelRunner…", section 2 (slot formula; slot == -1
  * is a padding row that writes nothing).
  *
- *   k, v            device, bf16, token i's row starts at k + i*k_tok_stride elements
- *                   and holds num_kv_heads*head_dim contiguous elements.
+ *   k, v            device, 16-bit elements (bf16 or fp16); token i's row starts at
+ *                   k + i*k_tok_stride elements and holds num_kv_heads*head_dim
+ *                   contiguous elements.
  *   k_tok_stride,
  *   v_tok_stride    token strides in ELEMENTS (>= num_kv_heads*head_dim).
- *   k_cache,v_cache device, bf16 [num_blocks, block_size, num_kv_heads, head_dim],
+ *   k_cache,v_cache device, the same element type [num_blocks, block_size, num_kv_heads,
+ *                   head_dim],
  *                   updated in place: row s of the [num_blocks*block_size,
  *                   num_kv_heads*head_dim] view receives token i when slot_mapping[i]==s.
  *   slot_mapping    device, int32 [num_tokens]; -1 = skip this token.
  *   num_tokens      >= 0 (0 launches nothing and returns PA_OK).
  *
  * The copy is bit-exact for any 16-bit element type (bf16 or fp16). head_dim 64 or 128.
- * Two tokens with the same slot race (the pages never produce that). A 16-byte vector path is used when k, v, both caches and both strides are
- * 16-byte aligned; otherwise a 2-byte path gives the same bytes.
+ * Two tokens with the same slot race (the pages never produce that). One warp moves one
+ * token's K or V row; 16-byte vectors are used when k, v, both caches and both strides
+ * are 16-byte aligned, otherwise 2-byte elements give the same bytes.
  */
 int pa_store_kvcache(const void* k, const void* v, int64_t k_tok_stride, int64_t v_tok_stride,
                      void* k_cache, void* v_cache, const int32_t* slot_mapping, int num_tokens,
