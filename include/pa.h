@@ -255,7 +255,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
  *                   overlap in time must use different workspaces.
  *
  * Arithmetic: 16-bit inputs widened exactly, fp32 products, fp32 online softmax and
- * accumulation, one round-to-nearest-even to the element type at the end.
+ * accumulation, one round-to-nearest-even to the element type at the end. Shapes that run
+ * on the tensor cores (3 to 8 query heads per KV head, or head_dim 64) also round each
+ * probability to the element type before the P V product (the softmax denominator stays
+ * fp32): at most 2^-9 relative per probability.
  *
  * Launch: a programmatic dependent launch. The grid may start while the previous kernel
  * on the stream is still running, provided that kernel lets its dependents start early
