@@ -293,8 +293,9 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  * sequence b (block_tables[b][p/bs]*bs + p%bs, p = context_lens[b]-1), which is how the
  * decode step builds it.
  *
- *   k_new, v_new    device, bf16; row b (start k_new + b*k_new_stride elements) holds
- *                   the num_kv_heads*head_dim values of sequence b's new token.
+ *   k_new, v_new    device, the element type of q (dtype); row b (start k_new +
+ *                   b*k_new_stride elements) holds the num_kv_heads*head_dim values of
+ *                   sequence b's new token.
  *   k_new_stride,
  *   v_new_stride    token strides in ELEMENTS, >= num_kv_heads*head_dim and multiples of 8
  *                   (k_new, v_new 16-byte aligned), else PA_ERR_ALIGN.
@@ -367,8 +368,8 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
  *   out             device, [cu_seqlens_q[num_seqs], num_heads, head_dim].
  *   q               device, same shape and element type as out.
  *   head_dim, dtype 64 or 128; PA_DTYPE_BF16 or PA_DTYPE_F16 (q, both caches and out).
- *   k_cache,v_cache device, bf16 caches that ALREADY hold every key/value row of the
- *                   call, the new tokens included (run pa_store_kvcache first).
+ *   k_cache,v_cache device caches of that element type that ALREADY hold every key/value
+ *                   row of the call, the new tokens included (run pa_store_kvcache first).
  *   block_tables    device, int32 [num_seqs, max_blocks_per_seq].
  *   cu_seqlens_q    device, int32 [num_seqs+1]; n_s = cu_seqlens_q[s+1]-cu_seqlens_q[s].
  *   cu_seqlens_k    device, int32 [num_seqs+1]; k_s = cu_seqlens_k[s+1]-cu_seqlens_k[s]
