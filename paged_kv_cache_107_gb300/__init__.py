@@ -400,8 +400,8 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
                    dev_err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Store of each sequence's new token plus decode, in one launch: the same result as
     pa_store_kvcache(k_new, v_new, ..., slot_mapping) then pa_decode(...). k_new, v_new
-    [B, Hk, D] of q's type (token stride a multiple of 8 elements); slot_mapping [B] int32, -1 or
-    the slot of position context_lens[b]-1 of sequence b."""
+    [B, Hk, D] of q's type (token stride a multiple of 8 elements); slot_mapping [B]
+    int32, -1 or the slot of position context_lens[b]-1 of sequence b."""
     _need16(q, "q", 3)
     for name, t, dt, nd in (("out", out, q.dtype, 3), ("q", q, q.dtype, 3),
                             ("k_cache", k_cache, q.dtype, 4),
