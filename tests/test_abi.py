@@ -139,3 +139,82 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
            "-L", libdir, f"-l{libname}", f"-Wl,-rpath,{libdir}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_c_program_runs_the_host_paths(lib, tmp_path):
+    """A C program, linked against the library, runs the entry points that need no GPU and
+    checks their results: version and status strings, empty batches and shape errors
+    answered before any CUDA call, and pa_staged_pack, whose packed runs, applied to a
+    host table, must equal the staged writes applied one after another in staging order
+    (later writes win where they overlap)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "host_paths.c"
+    src.write_text(r'''
+#include "pa.h"
+#include <stdio.h>
+#include <string.h>
+
+#define CHECK(c) do { if (!(c)) { printf("failed: %s (line %d)\n", #c, __LINE__); return 1; } } while (0)
+
+int main(void) {
+  CHECK(pa_version() >> 16 == 1);
+  CHECK(strcmp(pa_status_str(PA_OK), "PA_OK") == 0);
+  CHECK(pa_store_kvcache(NULL, NULL, 1024, 1024, NULL, NULL, NULL, 0, 8, 128, 16, 4, NULL,
+                         NULL) == PA_OK);
+  CHECK(pa_decode(NULL, NULL, NULL, NULL, NULL, 0, NULL, 0, 16, 8, 128, PA_DTYPE_BF16, 16, 4,
+                  0.f, 0, NULL, 0, NULL, NULL) == PA_OK);
+  CHECK(pa_decode(NULL, NULL, NULL, NULL, NULL, 1, NULL, 2, 12, 8, 128, PA_DTYPE_BF16, 16, 4,
+                  0.f, 0, NULL, 0, NULL, NULL) == PA_ERR_SHAPE);
+  CHECK(pa_prefill_varlen(NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL, 0, 0, 0, 16, 8, 128,
+                          PA_DTYPE_BF16, 256, 4, 1, 0.f, NULL, NULL) == PA_OK);
+  CHECK(pa_sample_workspace_size(-1) == 0);
+
+  /* staged writes, in staging order: later ones win where they overlap */
+  enum { R = 6, C = 12, W = 5 };
+  const int32_t rows[W] = {3, 0, 3, 5, 3};
+  const int32_t starts[W] = {4, 0, 2, 10, 6};
+  const int32_t lens[W] = {3, 2, 3, 2, 1};
+  const int32_t vals[11] = {10, 11, 12, 20, 21, 30, 31, 32, 40, 41, 50};
+  int32_t expect[R][C], got[R][C];
+  memset(expect, 0xff, sizeof expect);
+  memcpy(got, expect, sizeof got);
+  int v = 0;
+  for (int w = 0; w < W; ++w)
+    for (int i = 0; i < lens[w]; ++i) expect[rows[w]][starts[w] + i] = vals[v++];
+  unsigned char packed[1024] __attribute__((aligned(16)));
+  pa_staged_layout lay;
+  CHECK(pa_staged_pack_bound(W, 11, 4) <= sizeof packed);
+  CHECK(pa_staged_pack(rows, starts, lens, vals, W, 4, packed, sizeof packed, &lay) == PA_OK);
+  CHECK(lay.num_writes >= 1 && lay.num_writes <= W && lay.bytes <= (int64_t)sizeof packed);
+  const int32_t* pr = (const int32_t*)(packed + lay.rows_offset);
+  const int32_t* ps = (const int32_t*)(packed + lay.starts_offset);
+  const int32_t* po = (const int32_t*)(packed + lay.offsets_offset);
+  const int32_t* pv = (const int32_t*)(packed + lay.values_offset);
+  CHECK(lay.values_offset % 16 == 0 && po[0] == 0 && po[lay.num_writes] == lay.num_values);
+  for (int w = 0; w < lay.num_writes; ++w) {
+    CHECK(po[w + 1] >= po[w]);
+    for (int i = 0; i < po[w + 1] - po[w]; ++i) got[pr[w]][ps[w] + i] = pv[po[w] + i];
+  }
+  CHECK(memcmp(got, expect, sizeof got) == 0);
+  /* a buffer too small reports the size it needs */
+  pa_staged_layout small;
+  CHECK(pa_staged_pack(rows, starts, lens, vals, W, 4, packed, 8, &small) == PA_ERR_WORKSPACE);
+  CHECK(small.bytes == lay.bytes);
+  printf("ok %d runs\n", lay.num_writes);
+  return 0;
+}
+''')
+    exe = tmp_path / "host_paths"
+    libdir = os.path.dirname(lib_build.LIB_PATH)
+    libname = os.path.basename(lib_build.LIB_PATH)[3:-3]
+    cmd = [cc, "-std=gnu99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER),
+           str(src), "-o", str(exe), "-L", libdir, f"-l{libname}", f"-Wl,-rpath,{libdir}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("ok")
