@@ -642,6 +642,16 @@ def measure_prefix_sharing(dev, steps: int, warmup: int):
     return res
 
 
+def fit_stream_and_fixed(points):
+    """Least-squares line time = bytes / rate + fixed through (bytes, microseconds) points:
+    the streaming rate in GB/s and the fixed cost of a launch in microseconds."""
+    import numpy as np
+    x = np.array([a for a, _ in points], np.float64)
+    y = np.array([b for _, b in points], np.float64)
+    slope, icpt = np.polyfit(x, y, 1)  # us per byte, us
+    return {"stream_gbs": 1e-3 / slope, "fixed_us": float(icpt)}
+
+
 def measure_batch_sizes(dev, steps: int, warmup: int):
     """The fused decode step on the first B sequences of the decode-step workload (ctx
     U{100..2048}, H=16, H_kv=8, D=128, bs=256) for B = 1 .. 256: one launch at a time and
@@ -697,10 +707,7 @@ def measure_batch_sizes(dev, steps: int, warmup: int):
             pts.append((kv, per))
             pts_loop.append((kv, loop))
     for name, p in (("fit_per_launch", pts), ("fit_back_to_back", pts_loop)):
-        x = np.array([a for a, _ in p], np.float64)
-        y = np.array([b for _, b in p], np.float64)
-        slope, icpt = np.polyfit(x, y, 1)  # us per byte, us
-        res[name] = {"stream_gbs": 1e-3 / slope, "fixed_us": icpt}
+        res[name] = fit_stream_and_fixed(p)
     del kc, vc
     return res
 
