@@ -49,6 +49,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def burst_bf16_peak():
+    """The measured burst bf16 dense rate (a kernel timed alone), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def source_sha256(*names) -> str:
     """sha256 over the named csrc/ files, in order (the kernel and the headers it uses)."""
     h = hashlib.sha256()
@@ -80,22 +90,44 @@ def profile_value(sources, summary: str, key: str):
 
 
 SAMPLER_SOURCES = ("sample.cu", "pa_device.cuh")
+# ncu summaries of the fused decode step, by workload
+STEP_PROFILES = {"w2_qwen3_decode_b256": "decode_step_w2_qwen3_b256.md",
+                 "w3_long_context_b8": "decode_tc_w3_long_context_b8.md"}
 
 
-def kernel_traffic(sources, summary: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
-    kernel sources (sha256 recorded in the summary); otherwise None."""
+def kernel_traffic(sources, summary: str, workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if that summary was taken on the
+    current kernel sources (sha256 recorded in it), on this workload and of this kernel
+    (its `workload:` and `kernel:` lines); otherwise None."""
     path = os.path.join(ROOT, "profiles", summary)
     try:
         text = open(path).read()
         sha = source_sha256(*sources)
         m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
         m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-        if m_sha and m_b and m_sha.group(1) == sha:
+        m_w = re.search(r"^workload:\s*(\S+)\s*$", text, re.M)
+        m_k = re.search(r"^kernel:\s*(\S+)\s*$", text, re.M)
+        if (m_sha and m_b and m_w and m_k and m_sha.group(1) == sha
+                and m_w.group(1) == workload and m_k.group(1) == kernel):
             return float(m_b.group(1))
     except OSError:
         pass
     return None
+
+
+def decode_step_kernel(num_heads: int, num_kv_heads: int, head_dim: int) -> str:
+    """Which kernel runs the fused decode step for this shape (the routing rule of the
+    library's launcher: the CUDA-core kernel for 1-2 query heads per KV head at head_dim
+    128 when one head slab holds every KV head, the tensor-core kernel otherwise)."""
+    g = num_heads // num_kv_heads
+    one_slab = num_kv_heads in (1, 2, 4, 8)
+    if g >= 3 or not (head_dim == 128 and one_slab):
+        return "paged_decode_tc_kernel/fused"
+    return "paged_decode_kernel/fused"
+
+
+def decode_step_sources(kernel: str):
+    return DECODE_TC_SOURCES if kernel.startswith("paged_decode_tc_kernel") else DECODE_SOURCES
 
 
 class ClockSampler:
@@ -339,10 +371,50 @@ def prefill_flops(case) -> float:
     return 4.0 * case.num_heads * case.head_dim * pairs
 
 
-def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128, dtype=None):
+def prefill_cpu_baseline(case, seconds: float, threads: int = 0, stored=None):
+    """Time the fp64 oracle's prefill (as it stands) on a bounded sample of the chunked
+    prefill: (query token, head) rows in a seeded random order, in chunks, until about
+    `seconds` of wall time has passed. FLOPs count 4*D per unmasked (row, key) pair, as
+    the GPU figure does."""
+    import numpy as np
+    import oracle
+    cores = oracle.max_threads(threads)
+    ok, ov = stored if stored is not None else oracle.store_kvcache(
+        case.k_new, case.v_new, case.k_cache, case.v_cache, case.slot_mapping)
+    H, D = case.num_heads, case.head_dim
+    n = np.diff(case.cu_seqlens_q).astype(np.int64)
+    c = np.diff(case.cu_seqlens_k).astype(np.int64) - n
+    seq_of_tok = np.repeat(np.arange(len(n)), n)
+    keys_of_tok = c[seq_of_tok] + (np.arange(int(n.sum())) - np.repeat(case.cu_seqlens_q[:-1], n)) + 1
+    if not case.causal:
+        keys_of_tok = (c + n)[seq_of_tok]
+    order = np.random.default_rng(107005).permutation(int(n.sum()) * H)
+    chunk = 1024 if threads != 1 else 64
+    done_rows, done_pairs, t = 0, 0, 0.0
+    kb = ok.view(np.uint16)
+    vb = ov.view(np.uint16)
+    while t < seconds and done_rows < len(order):
+        rows = np.sort(order[done_rows:done_rows + chunk])
+        t0 = time.perf_counter()
+        oracle.prefill(case.q, kb, vb, case.block_tables, case.cu_seqlens_q, case.cu_seqlens_k,
+                       causal=case.causal, rows=rows, nthreads=threads)
+        t += time.perf_counter() - t0
+        done_rows += len(rows)
+        done_pairs += int(keys_of_tok[rows // H].sum())
+    flops = 4.0 * D * done_pairs
+    return {"tokens_per_s": done_rows / H / t, "gflops": flops / t / 1e9, "cores": cores,
+            "sample": f"{done_rows} (query token, head) rows of the {int(n.sum())}-token "
+                      f"chunk in a seeded random order ({done_pairs} unmasked row-key pairs), "
+                      f"fp64 oracle, {t:.1f} s"}
+
+
+def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128, dtype=None,
+                    cpu_seconds: float = 0.0):
     """Chunked-prefill step of workload 5: store of every new token, then causal prefill.
     Returns timings (CUDA events on the stream), TFLOP/s and the fraction of the measured
-    sustained bf16 tensor peak (fp16 has the same dense tensor rate)."""
+    bf16 tensor peak, burst (the prefill is timed alone, launch by launch) and sustained
+    (fp16 has the same dense tensor rate). With cpu_seconds > 0 the fp64 oracle's prefill is
+    timed beside it on the host cores (all of them, then one thread)."""
     import torch
     import paged_kv_cache_107_gb300 as pk
     from paged_kv_cache_107_gb300 import workloads
@@ -383,13 +455,17 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128
     pf_ms = statistics.median(b.elapsed_time(c) for _, b, c in ev)
     flops = prefill_flops(case)
     _, tflops_peak, src = measured_peaks()
+    tflops_burst, bsrc = burst_bf16_peak()
     nq = int(case.cu_seqlens_q[-1])
     store_bytes = nq * case.num_kv_heads * case.head_dim * 2 * 2 * 2
     res = {"workload": case.name, "new_tokens": nq, "flops": flops,
            "prefill_ms": pf_ms, "store_ms": st_ms,
            "tflops": flops / (pf_ms * 1e-3) / 1e12,
-           "tflops_frac": flops / (pf_ms * 1e-3) / 1e12 / tflops_peak,
-           "peak_tflops": tflops_peak, "peak_source": f"{src} bf16 dense (sustained)",
+           "tflops_frac": flops / (pf_ms * 1e-3) / 1e12 / tflops_burst,
+           "peak_tflops": tflops_burst, "peak_source": f"{bsrc} bf16 dense (burst: the prefill "
+                                                       "is timed alone, launch by launch)",
+           "tflops_frac_sustained": flops / (pf_ms * 1e-3) / 1e12 / tflops_peak,
+           "peak_tflops_sustained": tflops_peak,
            "tokens_per_s": nq / (pf_ms * 1e-3),
            "store_gbs": store_bytes / (st_ms * 1e-3) / 1e9}
     if head_dim == 128 and (dtype is None or dtype == torch.bfloat16):
@@ -399,13 +475,28 @@ def measure_prefill(dev, steps: int, warmup: int, pool_blocks=None, head_dim=128
             "kernel": "store_kvcache_kernel", "bound": "hbm", "unit": "GB/s",
             "achieved": res["store_gbs"], "peak": hbm_peak, "frac": res["store_gbs"] / hbm_peak,
             "peak_source": f"{hsrc} HBM copy GB/s", "alg_bytes_per_launch": store_bytes,
-            "traffic": kernel_traffic(STORE_SOURCES, "store_kvcache_w5_prefill.md")}
+            "traffic": kernel_traffic(STORE_SOURCES, "store_kvcache_w5_prefill.md", case.name,
+                                      "store_kvcache_kernel")}
     if head_dim == 128 and (dtype is None or dtype == torch.bfloat16):
         res["roofline"] = {
             "kernel": "paged_prefill_kernel", "bound": "tensor", "unit": "TFLOP/s",
-            "achieved": res["tflops"], "peak": tflops_peak, "frac": res["tflops_frac"],
-            "peak_source": f"{src} cuBLAS bf16 dense, sustained",
-            "traffic": kernel_traffic(PREFILL_SOURCES, "prefill_w5_chunked.md")}
+            "achieved": res["tflops"], "peak": tflops_burst, "frac": res["tflops_frac"],
+            "peak_source": f"{bsrc} cuBLAS bf16 dense, burst (kernel timed alone)",
+            "frac_of_sustained": res["tflops_frac_sustained"],
+            "traffic": kernel_traffic(PREFILL_SOURCES, "prefill_w5_chunked.md", case.name,
+                                      "paged_prefill_kernel")}
+    if cpu_seconds > 0:
+        import oracle
+        stored = oracle.store_kvcache(case.k_new, case.v_new, case.k_cache, case.v_cache,
+                                      case.slot_mapping)
+        cb = prefill_cpu_baseline(case, cpu_seconds, stored=stored)
+        c1 = prefill_cpu_baseline(case, max(cpu_seconds / 3, 1.0), threads=1, stored=stored)
+        res["cpu_baseline"] = {"value": cb["tokens_per_s"], "unit": "tokens/s",
+                               "gflops": cb["gflops"], "cores": cb["cores"], "kind": "oracle",
+                               "sample": cb["sample"],
+                               "single_thread": {"value": c1["tokens_per_s"], "unit": "tokens/s",
+                                                 "gflops": c1["gflops"], "cores": c1["cores"],
+                                                 "sample": c1["sample"]}}
     return res
 
 
@@ -482,7 +573,8 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
             "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9}
         summary = {"g8": "decode_tc_g8_w2_b256.md", "d64_bf16": "decode_tc_d64_w2_b256.md"}
         if tag in summary:
-            res["decode_step_" + tag]["traffic"] = kernel_traffic(DECODE_TC_SOURCES, summary[tag])
+            res["decode_step_" + tag]["traffic"] = kernel_traffic(
+                DECODE_TC_SOURCES, summary[tag], case.name, "paged_decode_tc_kernel/fused")
         del kc, vc, case
         if heads == 16 and only is None:
             res["prefill_" + tag] = measure_prefill(dev, steps=min(steps, 20), warmup=warmup,
@@ -491,6 +583,70 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
         res["decode_step_block_sizes"] = measure_block_sizes(dev, min(steps, 30), warmup)
         res["decode_step_batch_sizes"] = measure_batch_sizes(dev, min(steps, 30), warmup)
     return res
+
+
+def measure_long_context(dev, steps: int, warmup: int, pool_blocks=None):
+    """The long-context split-KV decode step (B=8, context U{32768..131072}, H=32, H_kv=8,
+    so 4 query heads per KV head, D=128, block size 256, the 4096-block pool): the fused
+    store + decode, one launch at a time (CUDA events per launch, for the roofline) and
+    back to back. Only 64 (sequence, KV head) pairs exist, so every sequence is split
+    across CTAs and combined in-kernel. K/V bytes (about 2.4 GB) exceed L2: no flush."""
+    import torch
+    import paged_kv_cache_107_gb300 as pk
+    from paged_kv_cache_107_gb300 import workloads
+    case = workloads.workload(3, poison=True, num_blocks=pool_blocks)
+    tot_ctx, kv_bytes, small_bytes, store_bytes = workload_summary(case)
+    H, Hk, D = case.num_heads, case.num_kv_heads, case.head_dim
+    kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+    q, kn, vn = case.q.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+    slots = torch.from_numpy(case.slot_mapping).to(dev)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    ctx = torch.from_numpy(case.context_lens).to(dev)
+    out = torch.empty_like(q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pk.DecodeWorkspace(case.num_seqs, H, Hk, D, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pk.pa_decode_step(out, q, kn, vn, kc, vc, slots, bt, ctx, workspace=ws, dev_err=err,
+                          stream=stream)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    lo, hi = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lo.record(stream)
+    for _ in range(steps):
+        step()
+    hi.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error bits {int(err.item())} in the long-context step")
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    loop_ms = lo.elapsed_time(hi) / steps
+    hbm_peak, _, peak_src = measured_peaks()
+    alg = kv_bytes + small_bytes + case.slot_mapping.nbytes + store_bytes // 2
+    kname = decode_step_kernel(H, Hk, D)
+    return {
+        "workload": case.name, "num_seqs": case.num_seqs, "total_context_tokens": tot_ctx,
+        "kv_bytes_per_step": kv_bytes, "step_us": ms * 1e3,
+        "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "seqs_per_s": case.num_seqs / (ms * 1e-3),
+        "loop_step_us": loop_ms * 1e3, "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9,
+        "pct_of_nominal_hbm": 100.0 * kv_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+        "roofline": {"kernel": kname, "bound": "hbm", "unit": "GB/s",
+                     "achieved": alg / (ms * 1e-3) / 1e9, "peak": hbm_peak,
+                     "peak_source": f"{peak_src} HBM copy GB/s",
+                     "frac": alg / (ms * 1e-3) / 1e9 / hbm_peak, "alg_bytes_per_launch": alg,
+                     "traffic": kernel_traffic(decode_step_sources(kname),
+                                               STEP_PROFILES.get(case.name, ""), case.name,
+                                               kname)},
+        "l2": "K/V read per step (~2.4 GB) >> 129 MB L2; no flush"}
 
 
 def measure_block_sizes(dev, steps: int, warmup: int):
@@ -959,7 +1115,9 @@ def run_ours(args):
     # q, o, block tables, context lengths, slots, and the new rows written to the cache
     step_alg_bytes = kv_bytes + small_bytes + case.slot_mapping.nbytes + store_bytes // 2
     achieved = step_alg_bytes / (step_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(DECODE_SOURCES, "decode_step_w2_qwen3_b256.md")
+    kname = decode_step_kernel(H, Hk, D)
+    traffic = kernel_traffic(decode_step_sources(kname), STEP_PROFILES.get(case.name, ""),
+                             case.name, kname)
 
     # ---- end to end through the public API with host buffers ---------------------------
     # every step uploads its inputs from pinned host memory (one packed copy) and copies its
@@ -1018,7 +1176,7 @@ def run_ours(args):
             "value": world * kv_bytes / (two_ms_step * 1e-3) / 1e9, "unit": "GB/s",
             "ms_per_step": two_ms_step, "kernels_ms": {"store": store_ms, "decode": decode_ms},
             "decode_achieved_gbs": (kv_bytes + small_bytes) / (decode_ms * 1e-3) / 1e9},
-        "roofline": {"kernel": "paged_decode_kernel (fused store)", "bound": "hbm",
+        "roofline": {"kernel": kname, "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak,
                      "peak_source": f"{peak_src} HBM copy GB/s",
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
@@ -1033,7 +1191,11 @@ def run_ours(args):
         "clocks": clk,
     }
     if not args.no_prefill:
-        line["prefill"] = measure_prefill(dev, steps=min(args.steps, 20), warmup=args.warmup)
+        line["long_context"] = measure_long_context(dev, steps=min(args.steps, 20),
+                                                    warmup=args.warmup)
+        cpu_s = 0.0 if (rank != 0 or args.no_cpu_baseline) else args.cpu_seconds / 2
+        line["prefill"] = measure_prefill(dev, steps=min(args.steps, 20), warmup=args.warmup,
+                                          cpu_seconds=cpu_s)
         line["staged_write"] = measure_staged(dev, steps=min(args.steps, 50), warmup=args.warmup)
         line["sampler"] = measure_sampler(dev, steps=min(args.steps, 50), warmup=args.warmup)
         line["variants"] = measure_variants(dev, steps=min(args.steps, 30), warmup=args.warmup)
@@ -1082,6 +1244,8 @@ def main():
                     help="time only the staged block-table writes (for profiler captures)")
     ap.add_argument("--batches-only", action="store_true",
                     help="time only the decode step at batch sizes 1..256")
+    ap.add_argument("--long-only", action="store_true",
+                    help="time only the long-context decode step (for profiler captures)")
     ap.add_argument("--prefix-only", action="store_true",
                     help="time only the prefix-sharing decode step at block sizes 16 and 256")
     ap.add_argument("--pool-blocks", type=int, default=None,
@@ -1118,6 +1282,13 @@ def main():
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         print(json.dumps(measure_batch_sizes(dev, args.steps, args.warmup)))
+    elif args.long_only:
+        import torch
+        import paged_kv_cache_107_gb300 as pk
+        pk.load_library()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_long_context(dev, args.steps, args.warmup, args.pool_blocks)))
     elif args.prefix_only:
         import torch
         import paged_kv_cache_107_gb300 as pk

@@ -343,7 +343,10 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
  *                   PA_ERR_WORKSPACE and launches nothing.
  *   First call      the first call on a device looks up the array's device address
  *                   (cudaGetSymbolAddress, with that device current); make that first
- *                   call before any stream capture.
+ *                   call before any stream capture. The address is kept per device and
+ *                   CUDA context: after the context is destroyed and recreated (for
+ *                   example by cudaDeviceReset) the next call looks it up again, so that
+ *                   call too should come before any capture.
  *   Sharing         every call on a device uses the same array and it keeps the last
  *                   call's contents; each call clears the arrival counters with an
  *                   asynchronous memset on `stream` before its launch. Calls that overlap

@@ -168,23 +168,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
 
 namespace pa {
 
-// pa_decode and pa_decode_step share validation and argument packing; `step` is null for
-// the plain call.
-struct StepInput {
-  const void* k_new;
-  const void* v_new;
-  int64_t k_new_stride;
-  int64_t v_new_stride;
-  const int32_t* slot_mapping;
-};
-
-static int decode_entry(void* out, const void* q, const void* k_cache, const void* v_cache,
-                        const int32_t* block_tables, int max_blocks_per_seq,
-                        const int32_t* context_lens, int num_seqs, int num_heads,
-                        int num_kv_heads, int head_dim, int dtype, int block_size,
-                        int64_t num_blocks, float scale, int grid_ctas, void* workspace,
-                        size_t workspace_bytes, int* dev_err, void* stream,
-                        const StepInput* step) {
+int decode_prepare(void* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                   int head_dim, int dtype, int block_size, int64_t num_blocks, float scale,
+                   int grid_ctas, int* dev_err, const DecodeStepInput* step, DecodeArgs* a,
+                   DeviceInfo* info, bool* nothing) {
+  *nothing = false;
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
       num_blocks <= 0 || max_blocks_per_seq < 0 || grid_ctas < 0)
     return PA_ERR_SHAPE;
@@ -197,7 +187,10 @@ static int decode_entry(void* out, const void* q, const void* k_cache, const voi
     const int64_t row = (int64_t)num_kv_heads * head_dim;
     if (step->k_new_stride < row || step->v_new_stride < row) return PA_ERR_SHAPE;
   }
-  if (num_seqs == 0) return PA_OK;
+  if (num_seqs == 0) {
+    *nothing = true;
+    return PA_OK;
+  }
   if (step) {
     if (!step->k_new || !step->v_new || !step->slot_mapping) return PA_ERR_NULL;
     // rows move with bulk copies: 16-byte aligned starts
@@ -209,48 +202,72 @@ static int decode_entry(void* out, const void* q, const void* k_cache, const voi
   if (max_blocks_per_seq > 0 && !block_tables) return PA_ERR_NULL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PA_ERR_ALIGN;
-  DeviceInfo info;
-  if (!current_device_info(&info)) return PA_ERR_CUDA;
-  const int max_ctas = decode_max_ctas(info);
+  if (!current_device_info(info)) return PA_ERR_CUDA;
   const bool auto_grid = grid_ctas == 0;
-  if (auto_grid) grid_ctas = info.num_sms;
-  if (grid_ctas > max_ctas) return PA_ERR_SHAPE;
-  size_t off_c, off_l, off_o, total;
-  decode_workspace_layout(num_seqs, num_heads, num_kv_heads, max_ctas, &off_c, &off_l, &off_o,
-                          &total);
-  if (!workspace || workspace_bytes < total) return PA_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return PA_ERR_ALIGN;
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  DecodeArgs a{};
-  a.out = out;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.max_blocks = max_blocks_per_seq;
-  a.num_seqs = num_seqs;
-  a.num_heads = num_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.block_size = block_size;
-  a.num_blocks = num_blocks;
-  a.scale_log2 = resolve_scale(scale, head_dim);
-  a.head_dim = head_dim;
-  a.f16 = dtype == PA_DTYPE_F16;
-  a.grid_ctas = grid_ctas;
-  a.min_tiles = auto_grid ? pa::kDecodeMinTilesPerCta : 1;
-  a.counters = reinterpret_cast<int*>(ws + off_c);
-  a.part_lse = reinterpret_cast<float*>(ws + off_l);
-  a.part_o = reinterpret_cast<float*>(ws + off_o);
-  a.dev_err = dev_err;
+  if (auto_grid) grid_ctas = info->num_sms;
+  if (grid_ctas > decode_max_ctas(*info)) return PA_ERR_SHAPE;
+  *a = DecodeArgs{};
+  a->out = out;
+  a->q = q;
+  a->k_cache = k_cache;
+  a->v_cache = v_cache;
+  a->block_tables = block_tables;
+  a->context_lens = context_lens;
+  a->max_blocks = max_blocks_per_seq;
+  a->num_seqs = num_seqs;
+  a->num_heads = num_heads;
+  a->num_kv_heads = num_kv_heads;
+  a->block_size = block_size;
+  a->num_blocks = num_blocks;
+  a->scale_log2 = resolve_scale(scale, head_dim);
+  a->head_dim = head_dim;
+  a->f16 = dtype == PA_DTYPE_F16;
+  a->grid_ctas = grid_ctas;
+  a->min_tiles = auto_grid ? kDecodeMinTilesPerCta : 1;
+  a->dev_err = dev_err;
   if (step) {
-    a.k_new = step->k_new;
-    a.v_new = step->v_new;
-    a.k_new_stride = step->k_new_stride;
-    a.v_new_stride = step->v_new_stride;
-    a.slot_mapping = step->slot_mapping;
-    return launch_decode_step(a, info, static_cast<cudaStream_t>(stream));
+    a->k_new = step->k_new;
+    a->v_new = step->v_new;
+    a->k_new_stride = step->k_new_stride;
+    a->v_new_stride = step->v_new_stride;
+    a->slot_mapping = step->slot_mapping;
   }
+  return PA_OK;
+}
+
+size_t decode_bind_workspace(DecodeArgs* a, unsigned char* ws, int layout_ctas) {
+  size_t off_c, off_l, off_o, total;
+  decode_workspace_layout(a->num_seqs, a->num_heads, a->num_kv_heads, layout_ctas, &off_c,
+                          &off_l, &off_o, &total);
+  a->counters = ws ? reinterpret_cast<int*>(ws + off_c) : nullptr;
+  a->part_lse = ws ? reinterpret_cast<float*>(ws + off_l) : nullptr;
+  a->part_o = ws ? reinterpret_cast<float*>(ws + off_o) : nullptr;
+  return total;
+}
+
+// pa_decode and pa_decode_step: the caller's workspace, laid out for the largest grid the
+// device allows (so one workspace serves every grid_ctas); `step` is null for the plain
+// call.
+static int decode_entry(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_heads,
+                        int num_kv_heads, int head_dim, int dtype, int block_size,
+                        int64_t num_blocks, float scale, int grid_ctas, void* workspace,
+                        size_t workspace_bytes, int* dev_err, void* stream,
+                        const DecodeStepInput* step) {
+  DecodeArgs a;
+  DeviceInfo info;
+  bool nothing = false;
+  const int rc = decode_prepare(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_heads, num_kv_heads, head_dim,
+                                dtype, block_size, num_blocks, scale, grid_ctas, dev_err, step,
+                                &a, &info, &nothing);
+  if (rc != PA_OK || nothing) return rc;
+  const size_t need =
+      decode_bind_workspace(&a, static_cast<unsigned char*>(workspace), decode_max_ctas(info));
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return PA_ERR_ALIGN;
+  if (step) return launch_decode_step(a, info, static_cast<cudaStream_t>(stream));
   return launch_decode(a, info, static_cast<cudaStream_t>(stream));
 }
 
@@ -276,7 +293,7 @@ int pa_decode_step(void* out, const void* q, const void* k_new, const void* v_ne
                    int num_heads, int num_kv_heads, int head_dim, int dtype, int block_size,
                    int64_t num_blocks, float scale, int grid_ctas, void* workspace,
                    size_t workspace_bytes, int* dev_err, void* stream) {
-  const pa::StepInput step{k_new, v_new, k_new_stride, v_new_stride, slot_mapping};
+  const pa::DecodeStepInput step{k_new, v_new, k_new_stride, v_new_stride, slot_mapping};
   return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                           context_lens, num_seqs, num_heads, num_kv_heads, head_dim, dtype,
                           block_size, num_blocks, scale, grid_ctas, workspace, workspace_bytes,

@@ -77,6 +77,30 @@ struct DecodeArgs {
   int* dev_err;
 };
 
+// The new tokens of pa_decode_step (null for pa_decode and pa_decode_noalloc).
+struct DecodeStepInput {
+  const void* k_new;
+  const void* v_new;
+  int64_t k_new_stride;
+  int64_t v_new_stride;
+  const int32_t* slot_mapping;
+};
+
+// Argument validation and packing shared by pa_decode, pa_decode_step and
+// pa_decode_noalloc (every check that does not concern the workspace). On PA_OK, *a holds
+// every field but the workspace pointers, *info describes the current device and the grid
+// is resolved (0 = one CTA per SM); *nothing is set when there is no sequence to launch.
+int decode_prepare(void* out, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                   int head_dim, int dtype, int block_size, int64_t num_blocks, float scale,
+                   int grid_ctas, int* dev_err, const DecodeStepInput* step, DecodeArgs* a,
+                   DeviceInfo* info, bool* nothing);
+// Points a's counters and partial-result slots into `ws`, laid out for layout_ctas CTAs
+// (decode_workspace_layout); returns the bytes that layout needs. ws may be null (only
+// the size is wanted then).
+size_t decode_bind_workspace(DecodeArgs* a, unsigned char* ws, int layout_ctas);
+
 // With the automatic grid, a CTA takes at least this many key tiles (64 KB of K and V
 // each at H_kv = 8): a short stream is then cut into fewer, longer CTA ranges, so that a
 // small batch's sequences are split into fewer segments to combine.

@@ -46,7 +46,8 @@ def test_fit_recovers_rate_and_fixed_cost():
 
 def test_profile_figures_only_while_sources_match(tmp_path, monkeypatch):
     """A committed ncu figure is reported only while the kernel sources it names hash to
-    the sha256 recorded beside it; any edit of those sources turns it into None."""
+    the sha256 recorded beside it, and a traffic figure only for the workload and kernel
+    the summary names; any edit of those sources turns it into None."""
     root = tmp_path / "repo"
     csrc = root / "paged_kv_cache_107_gb300" / "csrc"
     csrc.mkdir(parents=True)
@@ -56,14 +57,42 @@ def test_profile_figures_only_while_sources_match(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(root))
     sha = bench.source_sha256("k.cuh", "h.cuh")
     (root / "profiles" / "p.md").write_text(
-        f"source_sha256: {sha}\n| traffic_bytes_per_launch: 123456 | read + write |\n"
+        f"source_sha256: {sha}\nworkload: w_a\nkernel: kern/fused\n"
+        f"| traffic_bytes_per_launch: 123456 | read + write |\n"
         f"| inst_executed_per_launch: 789 | x |\n")
-    assert bench.kernel_traffic(("k.cuh", "h.cuh"), "p.md") == 123456.0
-    assert bench.profile_value(("k.cuh", "h.cuh"), "p.md", "inst_executed_per_launch") == 789.0
-    assert bench.kernel_traffic(("h.cuh", "k.cuh"), "p.md") is None   # order is part of it
+    src = ("k.cuh", "h.cuh")
+    assert bench.kernel_traffic(src, "p.md", "w_a", "kern/fused") == 123456.0
+    assert bench.kernel_traffic(src, "p.md", "w_b", "kern/fused") is None  # another workload
+    assert bench.kernel_traffic(src, "p.md", "w_a", "kern") is None        # another kernel
+    assert bench.profile_value(src, "p.md", "inst_executed_per_launch") == 789.0
+    assert bench.kernel_traffic(("h.cuh", "k.cuh"), "p.md", "w_a", "kern/fused") is None
     (csrc / "k.cuh").write_text("kernel v2\n")
-    assert bench.kernel_traffic(("k.cuh", "h.cuh"), "p.md") is None
-    assert bench.kernel_traffic(("k.cuh", "h.cuh"), "missing.md") is None
+    assert bench.kernel_traffic(src, "p.md", "w_a", "kern/fused") is None
+    assert bench.kernel_traffic(src, "missing.md", "w_a", "kern/fused") is None
+    assert bench.kernel_traffic(src, "", "w_a", "kern/fused") is None
+
+
+def test_decode_step_kernel_routing():
+    """The kernel the roofline names is the one the launcher picks for the shape."""
+    assert bench.decode_step_kernel(16, 8, 128) == "paged_decode_kernel/fused"
+    assert bench.decode_step_kernel(32, 8, 128) == "paged_decode_tc_kernel/fused"  # long ctx
+    assert bench.decode_step_kernel(64, 8, 128) == "paged_decode_tc_kernel/fused"
+    assert bench.decode_step_kernel(16, 8, 64) == "paged_decode_tc_kernel/fused"
+    assert bench.decode_step_kernel(32, 16, 128) == "paged_decode_tc_kernel/fused"
+    assert bench.decode_step_sources("paged_decode_tc_kernel/fused") == bench.DECODE_TC_SOURCES
+    assert bench.decode_step_sources("paged_decode_kernel/fused") == bench.DECODE_SOURCES
+
+
+def test_prefill_cpu_baseline_counts_pairs_of_its_sample():
+    """The CPU baseline's FLOPs are 4*D per unmasked pair of the rows it ran: with the
+    whole (tiny) chunk sampled they equal the chunk's FLOP count."""
+    case = workloads.prefill_case([0, 17, 30], [5, 9, 3], 4, 2, 64, 16, seed=5300,
+                                  poison=False)
+    r = bench.prefill_cpu_baseline(case, seconds=60.0, threads=1)
+    rows = int(case.cu_seqlens_q[-1]) * case.num_heads
+    assert r["sample"].startswith(f"{rows} ")
+    t = rows / case.num_heads / r["tokens_per_s"]
+    assert r["gflops"] * t * 1e9 == pytest.approx(bench.prefill_flops(case), rel=1e-9)
 
 
 def test_committed_profiles_name_existing_sources():

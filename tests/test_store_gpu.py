@@ -102,3 +102,20 @@ def test_store_full_size_decode_step():
     rng = np.random.default_rng(0)
     sample = rng.choice(fk.shape[0], 4096, replace=False)
     assert np.array_equal(fk[sample], ok2[sample]) and np.array_equal(fv[sample], ov2[sample])
+
+
+def test_store_full_chunked_prefill_workload_byte_for_byte():
+    """Every one of the chunked-prefill workload's 17,556 new tokens (32 sequences,
+    cached U{0..2048}, new U{100..1024}, block size 256, the 4096-block pool) stored in one
+    launch, then both whole caches compared byte for byte with the oracle's store.
+
+    The store's grid holds one resident wave of warps (6 blocks of 8 warps per SM), one
+    warp per K or V row; 35,112 rows are several per warp, so this is the size that takes
+    the kernel's grid-stride loop ("3.6 ModelRunner…", section 2: prepare_prefill builds
+    one slot per new token)."""
+    case = workloads.workload(5)
+    n_tok = int(case.cu_seqlens_q[-1])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 2 * n_tok > sms * 6 * 8, "the case must need more rows than the grid has warps"
+    assert np.all(case.slot_mapping >= 0)
+    _check_store(case)
