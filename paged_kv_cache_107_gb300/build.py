@@ -53,16 +53,26 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile csrc/*.cu for sm_103a and link lib/libpagedkv.so. Returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str = None) -> str:
+    """Compile csrc/*.cu for sm_103a and link lib/libpagedkv.so. Returns its path.
+
+    lib_path: build a separate library there instead (always rebuilt, objects beside it),
+    for example a test build with extra preprocessor flags; the in-tree library is left
+    alone."""
+    if lib_path is not None:
+        return _build_to(lib_path, lib_path + ".obj", verbose, extra_flags)
     if not force and up_to_date():
         return LIB_PATH
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    return _build_to(LIB_PATH, OBJ_DIR, verbose, extra_flags)
+
+
+def _build_to(lib_path: str, obj_dir: str, verbose: bool, extra_flags) -> str:
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     srcs = sources()
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *_flags(extra_flags), "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -76,14 +86,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, "-gencode", GENCODE, "-shared", "-Xcompiler", "-fPIC", "-o", tmp,
            *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

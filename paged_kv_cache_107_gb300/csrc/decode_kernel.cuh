@@ -657,6 +657,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+#ifdef PA_TEST_DELAY_LAST_TILE_CYCLES
+      // test build only: hold back the last tile's copies longer than the consumers' wait
+      // limit, so that their wait on it runs out (the copies are still issued, late, and
+      // drained below; nothing follows them in the ring)
+      if (it == n_tiles - 1) {
+        const long long t_hold = clock64();
+        while (clock64() - t_hold < (long long)(PA_TEST_DELAY_LAST_TILE_CYCLES)) {
+        }
+      }
+#endif
       unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
       if (lane == 0) {
         StageMeta& m = ctl.meta[s];
@@ -695,11 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_g2s(st + 2 * C::KV_BYTES, qsrc, C::Q_BYTES, &ctl.full[s]);
       }
     }
-    // drain: the last issued stages must land before the CTA may exit
+    // drain: the last issued stages must land before the CTA may exit (waited with the
+    // full limit even after a timeout elsewhere)
     const int64_t first_drain = n_tiles > C::STAGES ? n_tiles - C::STAGES : 0;
     for (int64_t it = first_drain; it < n_tiles; ++it) {
       const int s = (int)(it % C::STAGES);
-      mbar_wait(&ctl.full[s], (uint32_t)((it / C::STAGES) & 1), abort_flag);
+      mbar_wait_copies(&ctl.full[s], (uint32_t)((it / C::STAGES) & 1));
     }
     return;
   }

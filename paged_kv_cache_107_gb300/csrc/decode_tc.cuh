@@ -486,14 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++q_n;
       }
     }
-    // copies still in flight land before the producer leaves (bounded waits)
+    // copies still in flight land before the producer leaves (bounded waits, the full
+    // limit even after a timeout elsewhere)
     const int64_t first_drain = n_tiles > S ? n_tiles - S : 0;
     for (int64_t it = first_drain; it < n_tiles; ++it) {
       const int s = (int)(it % S);
-      mbar_wait(&ctl.full[s], (uint32_t)((it / S) & 1), abort_flag);
+      mbar_wait_copies(&ctl.full[s], (uint32_t)((it / S) & 1));
     }
     for (int n = q_n > TC::QS ? q_n - TC::QS : 0; n < q_n; ++n)
-      mbar_wait(&ctl.q_full[n % TC::QS], (uint32_t)((n / TC::QS) & 1), abort_flag);
+      mbar_wait_copies(&ctl.q_full[n % TC::QS], (uint32_t)((n / TC::QS) & 1));
     return;
   }
 

@@ -11,8 +11,12 @@ namespace pa {
 
 constexpr int kHeadDim = 128;
 // SM clock cycles before a wait is declared stuck (about 0.13 s at 2 GHz; a healthy wait in
-// these pipelines lasts microseconds), so a broken pipeline ends instead of hanging.
-constexpr long long kWaitCycles = 1ll << 28;
+// these pipelines lasts microseconds), so a broken pipeline ends instead of hanging. A test
+// build of the library defines PA_WAIT_CYCLES smaller to make a wait run out on purpose.
+#ifndef PA_WAIT_CYCLES
+#define PA_WAIT_CYCLES (1ll << 28)
+#endif
+constexpr long long kWaitCycles = PA_WAIT_CYCLES;
 
 __device__ __forceinline__ void set_dev_err(int* dev_err, int bit) {
   if (dev_err) atomicOr(dev_err, bit);
@@ -64,6 +68,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
+}
+
+// Bounded wait for this CTA's own copies in flight (before it exits): the full limit even
+// after another wait gave up, because a copy still landing in shared memory must not outlive
+// the CTA; copies end in microseconds unless the memory system is broken.
+__device__ __forceinline__ bool mbar_wait_copies(uint64_t* bar, uint32_t parity) {
+  return mbar_wait(bar, parity, nullptr);
 }
 
 // ---------------------------------------------------------------- bulk copies

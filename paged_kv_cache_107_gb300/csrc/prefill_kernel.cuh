@@ -222,6 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         load(true, it);
         if (it + 1 < n_all) load(false, it + 1);
       }
+      // the last copies of every stage land before the CTA may exit (the full limit even
+      // after a timeout elsewhere: a copy must not outlive the CTA's shared memory)
+      for (int it = n_all > kKStages ? n_all - kKStages : 0; it < n_all; ++it)
+        mbar_wait_copies(&sm.k_full[it % kKStages], (uint32_t)((it / kKStages) & 1));
+      for (int it = n_all > kVStages ? n_all - kVStages : 0; it < n_all; ++it)
+        mbar_wait_copies(&sm.v_full[it % kVStages], (uint32_t)((it / kVStages) & 1));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
