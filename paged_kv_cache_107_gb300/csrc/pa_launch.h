@@ -159,6 +159,7 @@ struct PrefillArgs {
   int head_dim;  // 64 or 128
   int f16;       // element type of q, caches, out: 0 = bf16, 1 = IEEE fp16
   int* dev_err;
+  int persistent;  // set by the launcher: 1 = one CTA per SM walking a sorted unit list
 };
 
 bool prefill_supported(int num_heads, int num_kv_heads, int block_size);

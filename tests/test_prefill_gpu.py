@@ -99,3 +99,46 @@ def test_full_chunked_prefill_workload_sampled():
             for h in (0, H - 1):
                 rows.add(t * H + h)
     run_prefill(case, rows=np.array(sorted(rows), np.int64))
+
+
+def _sampled_rows(case, n_random, seed, whole=()):
+    H = case.num_heads
+    rng = np.random.default_rng(seed)
+    total = int(case.cu_seqlens_q[-1])
+    rows = set(rng.choice(total * H, min(n_random, total * H), replace=False).tolist())
+    for s in whole:
+        for t in range(int(case.cu_seqlens_q[s]), int(case.cu_seqlens_q[s + 1])):
+            for h in range(H):
+                rows.add(t * H + h)
+    return np.array(sorted(rows), np.int64)
+
+
+def test_schedule_one_unit_per_cta_beyond_sort_limit():
+    """1,100 sequences (more than the in-kernel sort takes): the launcher runs one unit per
+    CTA on a (KV head, sequence, pair) grid. Every row is compared."""
+    rng = np.random.default_rng(1400)
+    cached = rng.integers(0, 41, 1100)
+    new = rng.integers(1, 4, 1100)
+    run_prefill(workloads.prefill_case(cached, new, 16, 8, 128, 16, seed=1401))
+
+
+def test_schedule_persistent_with_many_units_per_cta():
+    """8 query heads per KV head (16 positions per tile), 64 sequences of 512 new tokens:
+    8,192 units, about 54 per CTA on the persistent grid; sampled rows plus two whole
+    sequences."""
+    rng = np.random.default_rng(1500)
+    cached = rng.integers(0, 301, 64)
+    case = workloads.prefill_case(cached, [512] * 64, 64, 8, 128, 256, seed=1501)
+    run_prefill(case, rows=_sampled_rows(case, 4000, 1502, whole=(0, 63)))
+
+
+def test_schedule_one_unit_per_cta_beyond_pair_limit():
+    """8 query heads per KV head and up to 900 new tokens over 80 sequences: more possible
+    (sequence, pair) entries than the in-kernel sort takes, so one unit per CTA; sampled
+    rows plus the longest sequence whole."""
+    rng = np.random.default_rng(1600)
+    cached = rng.integers(0, 200, 80)
+    new = rng.integers(1, 901, 80)
+    new[5] = 900
+    case = workloads.prefill_case(cached, new, 64, 8, 128, 256, seed=1601)
+    run_prefill(case, rows=_sampled_rows(case, 3000, 1602, whole=(5,)))
