@@ -70,8 +70,13 @@ constexpr int kRows = 128;                 // query rows per tile (TMEM lanes)
 constexpr int kKeys = 128;                 // keys per K/V tile
 constexpr int kKStages = 3, kVStages = 2;  // ring depths
 constexpr int kHalf = 128 * 128;           // 128 rows x 64 dims: one swizzled column block
-constexpr int kThreads = 320;              // warps 0-3 tile A, 4-7 tile B, 8 TMA, 9 MMA
+constexpr int kThreads = 384;              // warps 0-3 tile A, 4-7 tile B, 8 TMA, 9 MMA, 10-11 idle
 constexpr int kTmaWarp = 8, kMmaWarp = 9;
+// Registers per thread after the set-up: the softmax warpgroups hold a 128-key score row
+// each; the third warpgroup (producer, MMA issuer, two idle warps) needs few. The sums per
+// SM sub-partition (one warp of each warpgroup) and per CTA match the launch's 168 x 384.
+constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= 168 * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows 256x
 // The in-kernel sort is used when the batch has at most kMaxSortSeqs sequences and
@@ -414,6 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &ctl.abort;
   const int n_units = ctl.n_units;
 
+  // Registers move from the control warpgroup (warps 8-11) to the softmax warpgroups; each
+  // branch then runs to its own end (teardown included), so the compiler keeps the two
+  // register budgets apart.
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -567,7 +577,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k + 1 < n_units) start_unit(recs[k + 1].nt);
       }
     }
+  }
+    // ---- teardown: every role is done with tensor memory
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+      umma::fence_after_sync();
+      umma::tmem_dealloc(tmem, kTmemCols);
+    }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------------ softmax warpgroups
     const int g = warp >> 2;      // query tile of this warpgroup
     const int r = tid & 127;      // row == TMEM lane
@@ -743,15 +762,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // unit, which follows these reads
       k = kn;
     }
+    // ---- teardown: every role is done with tensor memory
+    umma::fence_before_sync();
+    __syncthreads();
   }
 
-  // ---- teardown: every role is done with tensor memory ----------------------------------
-  umma::fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    umma::fence_after_sync();
-    umma::tmem_dealloc(tmem, kTmemCols);
-  }
 }
 
 template <int G, int D, bool F16>
