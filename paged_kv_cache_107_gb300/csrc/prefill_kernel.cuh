@@ -84,6 +84,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when th
 // records; otherwise the plain order.
 constexpr int kMaxSortSeqs = 1024;
 constexpr int kMaxSortPairs = 2048;
+constexpr int kRankSortMax = 512;  // up to this many entries a rank sort, else bitonic
 
 // TMEM columns: S (then P) of tile g at g*128, O of tile g at 256 + g*128.
 __host__ __device__ constexpr uint32_t col_s(int g) { return (uint32_t)(g * 128); }
@@ -175,11 +176,23 @@ __device__ __forceinline__ bool seq_ok(int n, int kv_len, int cap, int max_q) {
   return n >= 0 && kv_len >= n && kv_len <= cap && n <= max_q;
 }
 
-// Key tiles of the longer tile of a pair (the unit's cost), given its first new token i0.
+// Estimated time of a unit (the longest-first order's key), given its first new token i0:
+// a key-tile step that both tiles take costs about 2.1 us on GB300, a step of one tile
+// alone about 1.8 us, and a unit's start and end about 5 us (measured per unit with clock
+// traces of this kernel on the chunked-prefill workload); in units of 0.1 us.
 template <int P>
-__device__ __forceinline__ int pair_cost(int n, int kv_len, int i0, bool causal) {
-  const int keys = causal ? (kv_len - n) + min(n, i0 + 2 * P) : kv_len;
-  return (keys + kKeys - 1) / kKeys;
+__device__ __forceinline__ uint32_t pair_cost(int n, int kv_len, int i0, bool causal) {
+  const int c_len = kv_len - n;
+  int nt[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int rows = min(P, n - (i0 + g * P));
+    const int keys = rows <= 0 ? 0 : (causal ? c_len + i0 + g * P + rows : kv_len);
+    nt[g] = (keys + kKeys - 1) / kKeys;
+  }
+  const uint32_t both = (uint32_t)min(nt[0], nt[1]);
+  const uint32_t single = (uint32_t)abs(nt[0] - nt[1]);
+  return 21u * both + 18u * single + 50u;
 }
 
 // Key tiles each tile of a unit multiplies (causal: up to its last position); tile B may
@@ -243,7 +256,7 @@ __device__ void single_schedule(PrefillCtl& ctl, UnitRec* recs, const PrefillArg
 // the batch's bounds (num_seqs, max_seqlen_q, KV heads) guarantee that it fits.
 template <int P>
 __device__ void build_schedule(PrefillCtl& ctl, UnitRec* recs, unsigned char* scratch,
-                               const PrefillArgs& a) {
+                               const PrefillArgs& a, int cu_q0, int cu_k0) {
   const int tid = threadIdx.x;
   const int S = a.num_seqs, Hk = a.num_kv_heads;
   if (S > kMaxSortSeqs) {  // excluded by the launcher
@@ -261,7 +274,11 @@ __device__ void build_schedule(PrefillCtl& ctl, UnitRec* recs, unsigned char* sc
       scratch + ((3 * (kMaxSortSeqs + 1) * 4 + 15) & ~15));
   const int cap = a.max_blocks * a.block_size;
 
-  for (int i = tid; i <= S; i += kThreads) {
+  if (tid <= S) {  // loaded at kernel entry
+    cuq[tid] = cu_q0;
+    cuk[tid] = cu_k0;
+  }
+  for (int i = tid + kThreads; i <= S; i += kThreads) {
     cuq[i] = __ldg(a.cu_seqlens_q + i);
     cuk[i] = __ldg(a.cu_seqlens_k + i);
   }
@@ -325,25 +342,39 @@ __device__ void build_schedule(PrefillCtl& ctl, UnitRec* recs, unsigned char* sc
     const int n = cuq[s + 1] - cuq[s];
     const int kv = cuk[s + 1] - cuk[s];
     const uint32_t id = ((uint32_t)s << 12) | (uint32_t)qt;
-    const uint32_t cost = (uint32_t)pair_cost<P>(n, kv, qt * 2 * P, a.causal != 0);
+    const uint32_t cost = pair_cost<P>(n, kv, qt * 2 * P, a.causal != 0);
     keys[p] = ((unsigned long long)cost << 32) | (unsigned long long)(0xFFFFFFFFu - id);
   }
   for (int i = npairs + tid; i < n2; i += kThreads) keys[i] = 0ull;
   __syncthreads();
-  // bitonic sort, descending
-  for (int kk = 2; kk <= n2; kk <<= 1) {
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      for (int i = tid; i < n2; i += kThreads) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const unsigned long long x = keys[i], y = keys[ixj];
-          if ((i & kk) == 0 ? (x < y) : (x > y)) {
-            keys[i] = y;
-            keys[ixj] = x;
+  if (npairs <= kRankSortMax) {
+    // small batches: each key's place is the number of larger keys (keys are distinct),
+    // a few hundred shared-memory reads per thread instead of the network's barriers
+    unsigned long long* sorted = keys + n2;
+    for (int p = tid; p < npairs; p += kThreads) {
+      const unsigned long long x = keys[p];
+      int rank = 0;
+      for (int q = 0; q < npairs; ++q) rank += keys[q] > x;
+      sorted[rank] = x;
+    }
+    __syncthreads();
+    keys = sorted;
+  } else {
+    // bitonic sort, descending
+    for (int kk = 2; kk <= n2; kk <<= 1) {
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        for (int i = tid; i < n2; i += kThreads) {
+          const int ixj = i ^ jj;
+          if (ixj > i) {
+            const unsigned long long x = keys[i], y = keys[ixj];
+            if ((i & kk) == 0 ? (x < y) : (x > y)) {
+              keys[i] = y;
+              keys[ixj] = x;
+            }
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
   }
   // this CTA's units: the deal indices k with serp_index(k) < nunits form a prefix
@@ -381,6 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = tid & 31;
   const int H = a.num_heads;
   const bool causal = a.causal != 0;
+  // the schedule's first inputs, requested before the set-up below so that their latency
+  // overlaps it (entries past kThreads are loaded by the schedule itself)
+  int cu_q0 = 0, cu_k0 = 0;
+  if (a.persistent && tid <= a.num_seqs && a.num_seqs <= kMaxSortSeqs) {
+    cu_q0 = __ldg(a.cu_seqlens_q + tid);
+    cu_k0 = __ldg(a.cu_seqlens_k + tid);
+  }
 
   if (tid == 0) {
     mbar_init(&ctl.q_full[0], kRows);
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_relinquish();
   }
   __syncthreads();
-  if (a.persistent) build_schedule<P>(ctl, recs, &sm.k[0][0], a);
+  if (a.persistent) build_schedule<P>(ctl, recs, &sm.k[0][0], a, cu_q0, cu_k0);
   else single_schedule<P>(ctl, recs, a);
   // the schedule's scratch in the K ring was written through the generic proxy; TMA (the
   // async proxy) writes there next
@@ -637,11 +675,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         vbase = u.vbase;
         my_nt = nt_of(u.nt, g);
       }
+      // a few tiles before this unit's end: warm L2 with this row of the next unit's Q
+      // (copied in by cp.async at the last tile, when the Q buffer is free)
+      const int it_warm = kn < n_units ? max(0, my_nt - 3) : -1;
       float m_run = -INFINITY, l_run = 0.f;
       for (int it = 0; it < my_nt; ++it) {
         if (!mbar_wait(&ctl.s_full[g], (uint32_t)(sc & 1), abort_flag)) note_timeout(ctl, a.dev_err);
         ++sc;
         umma::fence_after_sync();
+        if (it == it_warm) {
+          const UnitRec& x = recs[kn];
+          const int qi = x.i0 + g * P + pos;
+          if (qi < x.n) {
+            const char* src = reinterpret_cast<const char*>(
+                static_cast<const uint16_t*>(a.q) + ((int64_t)(x.q0 + qi) * H + x.j * G + hh) * D);
+#pragma unroll
+            for (int b = 0; b < D * 2; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
+          }
+        }
         // the unit's last S product of this tile has completed: its Q buffer is free
         if (it == my_nt - 1 && kn < n_units) load_q(kn);
         float sv[kKeys];
@@ -741,21 +792,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = qi < u.n;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) +
                                             ((int64_t)(u.q0 + qi) * H + u.j * G + hh) * D);
+      float ob[D];  // the whole row at once: one tensor-memory round trip
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        float ob[32];
-        umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob);
-        umma::tmem_ld_wait();
-        if (row_ok) {
+      for (int c4 = 0; c4 < D / 32; ++c4) umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob + 32 * c4);
+      umma::tmem_ld_wait();
+      if (row_ok) {
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 pk;
-            pk.x = pack_elt2<F16>(ob[8 * q8 + 0] * inv, ob[8 * q8 + 1] * inv);
-            pk.y = pack_elt2<F16>(ob[8 * q8 + 2] * inv, ob[8 * q8 + 3] * inv);
-            pk.z = pack_elt2<F16>(ob[8 * q8 + 4] * inv, ob[8 * q8 + 5] * inv);
-            pk.w = pack_elt2<F16>(ob[8 * q8 + 6] * inv, ob[8 * q8 + 7] * inv);
-            dst[c4 * 4 + q8] = pk;
-          }
+        for (int q8 = 0; q8 < D / 8; ++q8) {
+          uint4 pk;
+          pk.x = pack_elt2<F16>(ob[8 * q8 + 0] * inv, ob[8 * q8 + 1] * inv);
+          pk.y = pack_elt2<F16>(ob[8 * q8 + 2] * inv, ob[8 * q8 + 3] * inv);
+          pk.z = pack_elt2<F16>(ob[8 * q8 + 4] * inv, ob[8 * q8 + 5] * inv);
+          pk.w = pack_elt2<F16>(ob[8 * q8 + 6] * inv, ob[8 * q8 + 7] * inv);
+          dst[q8] = pk;
         }
       }
       // the next unit's first P.V overwrites O_g only after this warpgroup's p_full of that
