@@ -260,9 +260,9 @@ __device__ __forceinline__ void combine_partials(const DecodeArgs& a, int b, int
   constexpr int CPL = D / 32;                 // combined dims per lane
   constexpr int HG = GMAX < 4 ? GMAX : 4;     // heads combined together
   // segments whose loads are in flight together, within the registers the kernel has
-  // left: four for groups of 1-2 heads (the CUDA-core kernel), two for four heads of 64
+  // left: eight for groups of 1-2 heads (the CUDA-core kernel), two for four heads of 64
   // dims, one for four heads of 128 dims (the tensor-core kernel)
-  constexpr int SU = HG <= 2 ? 4 : (HG * CPL <= 8 ? 2 : 1);
+  constexpr int SU = HG <= 2 ? 8 : (HG * CPL <= 8 ? 2 : 1);
   const int H = a.num_heads;
   const int SB = 32 / G;                      // segments per batch
   const int my_h = lane % G, my_j = lane / G;
