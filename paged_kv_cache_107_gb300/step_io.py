@@ -63,11 +63,17 @@ class DecodeStepPipeline:
     """Decode steps whose host<->device copies overlap the neighbouring steps' compute.
 
     `depth` sets of DecodeStepBuffers and output buffers are used in turn. Step i's inputs
-    move in on an upload stream while step i-1 computes, and its output moves out on a
-    download stream while step i+1 computes; CUDA events keep each buffer's uses in order
+    move in on an upload stream while earlier steps compute, and its output moves out on a
+    download stream while later steps compute; CUDA events keep each buffer's uses in order
     (a slot's device inputs are overwritten only after the step that read them finished,
     its device output only after the copy that read it out finished, its pinned host
     inputs only after their upload finished).
+
+    With group = g > 1 the steps are issued g at a time: the g uploads, then the g steps
+    back to back on the compute stream behind one event wait, then the g downloads. Inside
+    a group the steps follow each other directly, so each decode launch starts as the one
+    before it drains (dependent launches); an event wait between every two steps would
+    stop that. depth must hold two groups.
 
         pipe = DecodeStepPipeline(B, H, Hk, D, max_blocks)
         for i in range(n):
@@ -75,15 +81,17 @@ class DecodeStepPipeline:
             ...fill views...
             pipe.submit(i, run)          # run(dev_views, out) launches step i
             ...
-            host_out = pipe.output(i)    # step i's output on the host (waits for it)
+        pipe.flush()                     # issue a last, partial group
+        host_out = pipe.output(i)        # step i's output on the host (waits for it)
     """
 
     def __init__(self, num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
                  max_blocks: int, dtype: torch.dtype = torch.bfloat16, device="cuda",
-                 depth: int = 2, compute_stream=None):
-        if depth < 2:
-            raise ValueError("a pipeline needs at least two buffer sets")
+                 depth: int = 2, compute_stream=None, group: int = 1):
+        if group < 1 or depth < 2 * group:
+            raise ValueError("a pipeline needs room for two groups of steps")
         self.depth = depth
+        self.group = group
         self.device = torch.device(device)
         self.bufs = [DecodeStepBuffers(num_seqs, num_heads, num_kv_heads, head_dim, max_blocks,
                                        dtype=dtype, device=device) for _ in range(depth)]
@@ -94,17 +102,18 @@ class DecodeStepPipeline:
                         else torch.cuda.current_stream(self.device))
         self.up = torch.cuda.Stream(self.device)
         self.down = torch.cuda.Stream(self.device)
-        self.uploaded = [torch.cuda.Event() for _ in range(depth)]
-        self.computed = [torch.cuda.Event() for _ in range(depth)]
-        self.downloaded = [torch.cuda.Event() for _ in range(depth)]
-        self.used = [False] * depth
+        # per slot: the events of the last group that used it
+        self.uploaded = [None] * depth
+        self.computed = [None] * depth
+        self.downloaded = [None] * depth
+        self.pending = []  # (step, run) submitted but not yet issued
         self.h2d_bytes = self.bufs[0].nbytes
         self.d2h_bytes = self.out_host[0].numel() * self.out_host[0].element_size()
 
     def inputs(self, i: int) -> Dict[str, torch.Tensor]:
         """Pinned host views of step i's inputs, free to be written."""
         k = i % self.depth
-        if self.used[k]:
+        if self.uploaded[k] is not None:
             self.uploaded[k].synchronize()
         return self.bufs[k].host
 
@@ -114,36 +123,61 @@ class DecodeStepPipeline:
         self.down.wait_event(event)
 
     def submit(self, i: int, run) -> None:
-        """Upload step i's inputs, run it, and copy its output back, all asynchronously."""
-        k = i % self.depth
-        b = self.bufs[k]
-        if self.used[k]:
-            self.up.wait_event(self.computed[k])         # the last step that read these inputs
+        """Queue step i (its upload, its launch by run(dev_views, out), its download); a
+        full group is issued at once, asynchronously."""
+        self.pending.append((i, run))
+        if len(self.pending) == self.group:
+            self.flush()
+
+    def flush(self) -> None:
+        """Issue the queued steps (a group, or fewer at the end)."""
+        if not self.pending:
+            return
+        slots = [i % self.depth for i, _ in self.pending]
+        # uploads: each slot's device inputs are free once the step that last read them ran
+        for e in {id(self.computed[k]): self.computed[k] for k in slots
+                  if self.computed[k] is not None}.values():
+            self.up.wait_event(e)
         with torch.cuda.stream(self.up):
-            b.dev_buf.copy_(b.host_buf, non_blocking=True)
-        self.uploaded[k].record(self.up)
-        self.compute.wait_event(self.uploaded[k])
-        if self.used[k]:
-            self.compute.wait_event(self.downloaded[k])  # the last copy out of this output
+            for k in slots:
+                self.bufs[k].dev_buf.copy_(self.bufs[k].host_buf, non_blocking=True)
+        up_ev = torch.cuda.Event()
+        up_ev.record(self.up)
+        # the steps, back to back behind one wait (and the last copies out of their outputs)
+        self.compute.wait_event(up_ev)
+        for e in {id(self.downloaded[k]): self.downloaded[k] for k in slots
+                  if self.downloaded[k] is not None}.values():
+            self.compute.wait_event(e)
         with torch.cuda.stream(self.compute):
-            run(b.dev, self.out_dev[k])
-        self.computed[k].record(self.compute)
-        self.down.wait_event(self.computed[k])
+            for i, run in self.pending:
+                k = i % self.depth
+                run(self.bufs[k].dev, self.out_dev[k])
+        comp_ev = torch.cuda.Event()
+        comp_ev.record(self.compute)
+        # downloads
+        self.down.wait_event(comp_ev)
         with torch.cuda.stream(self.down):
-            self.out_host[k].copy_(self.out_dev[k], non_blocking=True)
-        self.downloaded[k].record(self.down)
-        self.used[k] = True
+            for k in slots:
+                self.out_host[k].copy_(self.out_dev[k], non_blocking=True)
+        down_ev = torch.cuda.Event()
+        down_ev.record(self.down)
+        for k in slots:
+            self.uploaded[k], self.computed[k], self.downloaded[k] = up_ev, comp_ev, down_ev
+        self.pending = []
 
     def output(self, i: int) -> torch.Tensor:
-        """Step i's output in pinned host memory (valid until step i + depth is submitted)."""
+        """Step i's output in pinned host memory (valid until step i + depth is submitted);
+        issues the queued steps first if step i is among them."""
+        if any(j == i for j, _ in self.pending):
+            self.flush()
         k = i % self.depth
         self.downloaded[k].synchronize()
         return self.out_host[k]
 
     def join(self, stream=None) -> None:
-        """Make `stream` (default: the compute stream) wait for every submitted copy."""
+        """Issue the queued steps and make `stream` (default: the compute stream) wait for
+        every submitted copy."""
+        self.flush()
         s = stream if stream is not None else self.compute
-        for k in range(self.depth):
-            if self.used[k]:
-                s.wait_event(self.uploaded[k])
-                s.wait_event(self.downloaded[k])
+        for e in {id(x): x for x in self.uploaded + self.downloaded if x is not None}.values():
+            s.wait_event(e)

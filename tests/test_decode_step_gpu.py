@@ -208,11 +208,12 @@ def test_step_on_packed_buffers_equals_separate_tensors():
     assert torch.equal(kc.view(torch.int16), ref_dc.k_cache.view(torch.int16))
 
 
-def test_pipelined_steps_equal_sequential_steps():
+@pytest.mark.parametrize("group", [1, 2, 3])
+def test_pipelined_steps_equal_sequential_steps(group):
     """Five decode steps (each sequence one token longer per step, fresh q / k_new / v_new)
     through DecodeStepPipeline, with uploads and downloads overlapping the neighbouring
-    steps, give step by step the bits of the same five steps run one after another; the
-    caches end equal."""
+    steps and the steps issued `group` at a time (a partial group at the end), give step by
+    step the bits of the same five steps run one after another; the caches end equal."""
     from paged_kv_cache_107_gb300.step_io import DecodeStepPipeline
     lens0 = [5, 260, 1, 999, 0, 77, 300, 16]
     B, H, Hk, D, bs, n_steps = len(lens0), 16, 8, 128, 16, 5
@@ -243,7 +244,7 @@ def test_pipelined_steps_equal_sequential_steps():
         pk.pa_decode_step(o, d["q"], d["k_new"], d["v_new"], kc_b, vc_b, d["slot_mapping"],
                           d["block_tables"], d["context_lens"], dev_err=err)
         ref.append(o.cpu())
-    pipe = DecodeStepPipeline(B, H, Hk, D, bt.shape[1])
+    pipe = DecodeStepPipeline(B, H, Hk, D, bt.shape[1], depth=2 * group, group=group)
 
     def run(d, out):
         pk.pa_decode_step(out, d["q"], d["k_new"], d["v_new"], kc_a, vc_a, d["slot_mapping"],
