@@ -31,8 +31,9 @@
 //  * TMA: K and V are described by 4-D tensor maps over [num_blocks, block_size, H_kv, D];
 //    a box of (64 dims x 1 head x R rows x 1 block), 128-byte swizzled, takes the physical
 //    block id from the block table as a coordinate. A K/V tile is 128 keys (R = 128 when
-//    block_size >= 128, else several blocks). K has a 3-deep ring, V a 2-deep one; K runs
-//    one tile ahead of V.
+//    block_size >= 128, else several blocks, one box per block, copied by one lane each).
+//    The producer warp reads each tile's block ids two tiles ahead of their first use. K
+//    has a 3-deep ring, V a 2-deep one; K runs one tile ahead of V.
 //  * tcgen05.mma (kind::f16, 16-bit operands, fp32 accumulators in tensor memory, all 512
 //    columns): S_g = Q_g K^T (A = Q and B = K from shared memory, K-major) in 128 columns per
 //    tile; the softmax writes P back over S as packed 16-bit values and O_g += P V reads P
@@ -464,63 +465,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA producer
+    // The whole warp walks the stream of key tiles (units in order, tiles in order): lane b
+    // reads box b's block id, two tiles ahead of the K load that first needs it (the V load
+    // of the same tile reuses it), so the table's latency stays off the copies' path; lane
+    // 0 waits for free stages and issues the copies.
     if (lane == 0) {
       umma::prefetch_tmap(&tm_k);
       umma::prefetch_tmap(&tm_v);
-      const int bs = a.block_size;
-      const int box_rows = bs < kKeys ? bs : kKeys;
-      const int boxes = kKeys / box_rows;
-      int kl = 0, vl = 0;  // K and V loads issued so far (ring slot and phase)
-      for (int k = 0; k < n_units; ++k) {
-        const UnitRec& u = recs[k];
-        const int n_all = nt_all(u.nt);
-        const int kv_len = u.kv_len, hj = u.j;
-        const int32_t* table = a.block_tables + (int64_t)u.s * a.max_blocks;
-        auto load = [&](bool is_v, int it) {
-          const int stages = is_v ? kVStages : kKStages;
-          const int cnt = is_v ? vl++ : kl++;
-          const int st = cnt % stages;
-          uint64_t* empty = is_v ? &ctl.v_empty[st] : &ctl.k_empty[st];
-          uint64_t* full = is_v ? &ctl.v_full[st] : &ctl.k_full[st];
-          if (cnt >= stages &&
-              !mbar_wait(empty, (uint32_t)(((cnt / stages) - 1) & 1), abort_flag))
-            note_timeout(ctl, a.dev_err);
-          const int t0 = it * kKeys;
-          int blk[kKeys / 8];  // at most 16 boxes (block_size 8)
-          uint32_t bytes = 0;
-          for (int bx = 0; bx < boxes; ++bx) {
-            const int key0 = t0 + bx * box_rows;
-            blk[bx] = -1;
-            if (key0 < kv_len) {
-              const int id = __ldg(table + key0 / bs);
-              if (id >= 0 && (int64_t)id < a.num_blocks) {
-                blk[bx] = id;
-                bytes += (uint32_t)NH * box_rows * 128u;
-              } else if (!is_v) {
-                set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
-              }
-            }
-          }
-          const int row0 = (bs > kKeys) ? (t0 % bs) : 0;
-          unsigned char* dst = is_v ? sm.v[st] : sm.k[st];
-          const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-          mbar_arrive_expect_tx(full, bytes);
-          for (int bx = 0; bx < boxes; ++bx) {
-            if (blk[bx] < 0) continue;
-            for (int h2 = 0; h2 < NH; ++h2)
-              umma::tma_load_4d(dst + h2 * kHalf + bx * box_rows * 128, map, h2 * 64, hj, row0,
-                                blk[bx], full);
-          }
-        };
-        // K runs one tile ahead of V: S(i+1) is issued right after PV(i)
-        load(false, 0);
-        for (int it = 0; it < n_all; ++it) {
-          load(true, it);
-          if (it + 1 < n_all) load(false, it + 1);
-        }
+    }
+    const int bs = a.block_size;
+    const int box_rows = bs < kKeys ? bs : kKeys;
+    const int boxes = kKeys / box_rows;  // at most 16 (block_size 8)
+    // this lane's block id of tile `it` of unit k: -1 past the keys (or past the stream),
+    // -2 out of the pool
+    auto read_id = [&](int k, int it) {
+      if (k >= n_units || lane >= boxes) return -1;
+      const UnitRec& u = recs[k];
+      const int key0 = it * kKeys + lane * box_rows;
+      if (key0 >= u.kv_len) return -1;
+      const int id = __ldg(a.block_tables + (int64_t)u.s * a.max_blocks + key0 / bs);
+      return (id >= 0 && (int64_t)id < a.num_blocks) ? id : -2;
+    };
+    auto advance = [&](int& k, int& it) {
+      if (k < n_units && ++it >= nt_all(recs[k].nt)) {
+        ++k;
+        it = 0;
       }
-      // the last copies of every stage land before the CTA may exit (the full limit even
-      // after a timeout elsewhere: a copy must not outlive the CTA's shared memory)
+    };
+    int kl = 0, vl = 0;  // K and V loads issued so far (ring slot and phase)
+    // lane-held ids of the current tile, the next one and the one after (being read)
+    int k1 = 0, it1 = 0;
+    advance(k1, it1);
+    int k2 = k1, it2 = it1;
+    advance(k2, it2);
+    int id0 = read_id(0, 0), id1 = read_id(k1, it1), id2 = read_id(k2, it2);
+    auto load = [&](bool is_v, int hj, int it, int id) {
+      const int stages = is_v ? kVStages : kKStages;
+      const int cnt = is_v ? vl++ : kl++;
+      const int st = cnt % stages;
+      uint64_t* empty = is_v ? &ctl.v_empty[st] : &ctl.k_empty[st];
+      uint64_t* full = is_v ? &ctl.v_full[st] : &ctl.k_full[st];
+      if (lane == 0 && cnt >= stages &&
+          !mbar_wait(empty, (uint32_t)(((cnt / stages) - 1) & 1), abort_flag))
+        note_timeout(ctl, a.dev_err);
+      if (!is_v && __any_sync(0xffffffffu, id == -2) && lane == 0)
+        set_dev_err(a.dev_err, PA_DEV_ERR_BLOCK_ID);
+      const uint32_t valid = __ballot_sync(0xffffffffu, id >= 0);  // boxes with a block
+      if (lane == 0)
+        mbar_arrive_expect_tx(full, (uint32_t)__popc(valid) * NH * box_rows * 128u);
+      __syncwarp();  // the stage is free and its bytes are expected: each box's lane copies
+      if (id >= 0) {
+        const int row0 = (bs > kKeys) ? ((it * kKeys) % bs) : 0;
+        unsigned char* dst = (is_v ? sm.v[st] : sm.k[st]) + lane * box_rows * 128;
+        const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+        for (int h2 = 0; h2 < NH; ++h2)
+          umma::tma_load_4d(dst + h2 * kHalf, map, h2 * 64, hj, row0, id, full);
+      }
+      __syncwarp();
+    };
+    for (int k = 0; k < n_units; ++k) {
+      const int n_all = nt_all(recs[k].nt);
+      const int hj = recs[k].j;
+      // K runs one tile ahead of V: S(i+1) is issued right after PV(i)
+      load(false, hj, 0, id0);
+      for (int it = 0; it < n_all; ++it) {
+        load(true, hj, it, id0);
+        if (it + 1 < n_all) load(false, hj, it + 1, id1);
+        // shift the window one tile along the stream
+        id0 = id1;
+        id1 = id2;
+        advance(k2, it2);
+        id2 = read_id(k2, it2);
+      }
+    }
+    // the last copies of every stage land before the CTA may exit (the full limit even
+    // after a timeout elsewhere: a copy must not outlive the CTA's shared memory)
+    if (lane == 0) {
       for (int c = kl > kKStages ? kl - kKStages : 0; c < kl; ++c)
         mbar_wait_copies(&ctl.k_full[c % kKStages], (uint32_t)((c / kKStages) & 1));
       for (int c = vl > kVStages ? vl - kVStages : 0; c < vl; ++c)
