@@ -24,16 +24,18 @@
 //    exceed what the in-kernel sort and the records hold run the same code one unit per
 //    CTA, on a grid of (KV head, sequence, pair), latest pairs first.
 //  * Units follow each other without draining the pipeline: the K/V ring runs on across
-//    units, each softmax warpgroup loads its next unit's Q (cp.async) as soon as the last
-//    S product of its current unit has completed, and the next unit's first S products are
-//    issued right after the current unit's last P.V products, while the softmax
-//    warpgroups write out the finished rows.
+//    units, a Q warp copies a tile's next Q (TMA, one box per 64 dims of the tile's 128/G
+//    positions x G heads) as soon as the tile's last S product of the current unit has
+//    completed, and the next unit's first S products are issued right after the current
+//    unit's last P.V products, while the softmax warpgroups write out the finished rows
+//    (32-byte stores).
 //  * TMA: K and V are described by 4-D tensor maps over [num_blocks, block_size, H_kv, D];
 //    a box of (64 dims x 1 head x R rows x 1 block), 128-byte swizzled, takes the physical
 //    block id from the block table as a coordinate. A K/V tile is 128 keys (R = 128 when
 //    block_size >= 128, else several blocks, one box per block, copied by one lane each).
 //    The producer warp reads each tile's block ids two tiles ahead of their first use. K
-//    has a 3-deep ring, V a 2-deep one; K runs one tile ahead of V.
+//    has a 2-deep ring, V a 3-deep one (a V tile waits longest: from its copy to the P.V
+//    product of both tiles); K runs one tile ahead of V.
 //  * tcgen05.mma (kind::f16, 16-bit operands, fp32 accumulators in tensor memory, all 512
 //    columns): S_g = Q_g K^T (A = Q and B = K from shared memory, K-major) in 128 columns per
 //    tile; the softmax writes P back over S as packed 16-bit values and O_g += P V reads P
@@ -62,6 +64,7 @@
 
 #include "pa_device.cuh"
 #include "pa_launch.h"
+#include "tensor_map.h"
 #include "umma.cuh"
 
 namespace pa {
@@ -69,12 +72,12 @@ namespace {
 
 constexpr int kRows = 128;                 // query rows per tile (TMEM lanes)
 constexpr int kKeys = 128;                 // keys per K/V tile
-constexpr int kKStages = 3, kVStages = 2;  // ring depths
+constexpr int kKStages = 2, kVStages = 3;  // ring depths
 constexpr int kHalf = 128 * 128;           // 128 rows x 64 dims: one swizzled column block
-constexpr int kThreads = 384;              // warps 0-3 tile A, 4-7 tile B, 8 TMA, 9 MMA, 10-11 idle
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 384;  // warps 0-3 tile A, 4-7 tile B, 8 K/V TMA, 9 MMA, 10 Q, 11 idle
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kQWarp = 10;
 // Registers per thread after the set-up: the softmax warpgroups hold a 128-key score row
-// each; the third warpgroup (producer, MMA issuer, two idle warps) needs few. The sums per
+// each; the third warpgroup (producers, MMA issuer, an idle warp) needs few. The sums per
 // SM sub-partition (one warp of each warpgroup) and per CTA match the launch's 168 x 384.
 constexpr int kSoftmaxRegs = 200, kControlRegs = 104;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= 168 * kThreads, "register split");
@@ -106,7 +109,8 @@ struct UnitRec {
 // Barriers and schedule state; first in shared memory, then the unit records, then the
 // tiles from the next 1024-byte boundary (128-byte swizzle atoms are 1024 bytes).
 struct PrefillCtl {
-  uint64_t q_full[2];          // [tile] the Q rows of a unit landed (128 arrivals)
+  uint64_t q_full[2];          // [tile] the Q rows of a unit landed
+  uint64_t q_empty[2];         // [tile] the last S product of a unit done: Q buffer free
   uint64_t k_full[kKStages];
   uint64_t k_empty[kKStages];  // S products of that K stage done
   uint64_t v_full[kVStages];
@@ -139,6 +143,12 @@ constexpr size_t prefill_smem_bytes() {
   return 1023 /* alignment of the tiles */ + kCtlBytes + kRecBytes + sizeof(PrefillTiles<D>);
 }
 
+// Rows of q that the Q tensor map spans (a bound on the batch's tokens known to the host).
+__host__ __device__ inline int64_t q_map_rows(const PrefillArgs& a) {
+  const int64_t r = (int64_t)a.num_seqs * a.max_seqlen_q;
+  return r < INT32_MAX ? r : INT32_MAX;
+}
+
 __device__ __forceinline__ void note_timeout(PrefillCtl& c, int* dev_err) {
   c.abort = 1;
   set_dev_err(dev_err, PA_DEV_ERR_TIMEOUT);
@@ -154,6 +164,15 @@ __device__ __forceinline__ uint32_t pack_elt2(float lo, float hi) {
   } else {
     return f32x2_to_bf16x2(lo, hi);
   }
+}
+
+// true in one lane of the (fully active) warp: the lowest
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // 16-byte global -> shared copy (cp.async, cached in L2 only); src_bytes 0 writes 16 zeros.
@@ -398,7 +417,8 @@ __device__ void build_schedule(PrefillCtl& ctl, UnitRec* recs, unsigned char* sc
 template <int G, int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_q, const PrefillArgs a) {
   constexpr int P = kRows / G;  // query positions per tile
   constexpr int NH = D / 64;    // 64-dim swizzled column blocks per row
   using Tiles = PrefillTiles<D>;
@@ -422,8 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    mbar_init(&ctl.q_full[0], kRows);
-    mbar_init(&ctl.q_full[1], kRows);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&ctl.q_full[g], 1);
+      mbar_init(&ctl.q_empty[g], 1);
+    }
     for (int b = 0; b < kKStages; ++b) {
       mbar_init(&ctl.k_full[b], 1);
       mbar_init(&ctl.k_empty[b], 1);
@@ -548,30 +570,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop (its descriptors are warp-uniform); one elected lane
+    // issues the products and commits.
+    {
       constexpr uint32_t idesc_s = umma::idesc_f32acc(kRows, kKeys, false, F16);
       constexpr uint32_t idesc_o = umma::idesc_f32acc(kRows, D, true, F16);
       int kc = 0, vc = 0;      // K and V loads consumed
       int qc[2] = {0, 0};      // Q tiles consumed, per tile slot
       int pc[2] = {0, 0};      // P tiles consumed, per tile slot
+      auto commit1 = [&](uint64_t* bar) {  // arrival on bar once the products so far are done
+        if (elect_one()) umma::commit(bar);
+        __syncwarp();
+      };
       auto issue_s = [&](int g, int kstage) {  // S_g = Q_g K^T
-        const uint32_t k_addr = smem_u32(sm.k[kstage]);
-        const uint32_t q_addr = smem_u32(sm.q[g]);
+        // descriptors of the K-slice kk: the tile's base descriptor plus the slice's offset
+        // in 16-byte units (the address field cannot carry: shared addresses are < 256 KB)
+        const uint64_t qd = umma::smem_desc(smem_u32(sm.q[g]), 16, 1024);
+        const uint64_t kd = umma::smem_desc(smem_u32(sm.k[kstage]), 16, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma::mma_bf16(tmem + col_s(g), umma::smem_desc(q_addr + off, 16, 1024),
-                         umma::smem_desc(k_addr + off, 16, 1024), idesc_s, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off16 = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            umma::mma_bf16(tmem + col_s(g), qd + off16, kd + off16, idesc_s, kk > 0);
+          }
+          umma::commit(&ctl.s_full[g]);
         }
-        umma::commit(&ctl.s_full[g]);
+        __syncwarp();
       };
       auto issue_pv = [&](int g, int vstage, bool first) {  // O_g (+)= P_g V, P from TMEM
-        const uint32_t v_addr = smem_u32(sm.v[vstage]);
+        const uint64_t vd = umma::smem_desc(smem_u32(sm.v[vstage]), kHalf, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma::mma_bf16_ts(tmem + col_o(g), tmem + col_s(g) + kk * 8,
-                            umma::smem_desc(v_addr + kk * 16 * 128, kHalf, 1024), idesc_o,
-                            !first || (kk > 0));
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            umma::mma_bf16_ts(tmem + col_o(g), tmem + col_s(g) + kk * 8,
+                              vd + ((kk * 16 * 128) >> 4), idesc_o, !first || (kk > 0));
+        }
+        __syncwarp();
       };
       auto wait_k = [&]() {
         if (!mbar_wait(&ctl.k_full[kc % kKStages], (uint32_t)((kc / kKStages) & 1), abort_flag))
@@ -589,9 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         wait_k();
 #pragma unroll
-        for (int g = 0; g < 2; ++g)
-          if (nt_of(nt, g) > 0) issue_s(g, kc % kKStages);
-        umma::commit(&ctl.k_empty[kc % kKStages]);
+        for (int g = 0; g < 2; ++g) {
+          if (nt_of(nt, g) == 0) continue;
+          issue_s(g, kc % kKStages);
+          if (nt_of(nt, g) == 1) commit1(&ctl.q_empty[g]);  // the unit's last S_g
+        }
+        commit1(&ctl.k_empty[kc % kKStages]);
         ++kc;
       };
       if (n_units > 0) start_unit(recs[0].nt);
@@ -615,24 +652,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma::fence_after_sync();
             issue_pv(g, vc % kVStages, it == 0);
-            if (it == ntg - 1) umma::commit(&ctl.o_done[g]);
+            if (it == ntg - 1) commit1(&ctl.o_done[g]);
             if (it + 1 < ntg) {
               if (!k_ready) {
                 wait_k();
                 k_ready = true;
               }
               issue_s(g, kc % kKStages);
+              if (it + 2 == ntg) commit1(&ctl.q_empty[g]);  // the unit's last S_g
             }
           }
-          umma::commit(&ctl.v_empty[vc % kVStages]);
+          commit1(&ctl.v_empty[vc % kVStages]);
           ++vc;
           if (k_ready) {
-            umma::commit(&ctl.k_empty[kc % kKStages]);
+            commit1(&ctl.k_empty[kc % kKStages]);
             ++kc;
           }
         }
         // the next unit's first S products follow this unit's last P.V products
         if (k + 1 < n_units) start_unit(recs[k + 1].nt);
+      }
+    }
+  } else if (warp == kQWarp) {
+    // ------------------------------------------------------------------ Q loader
+    // Tile g of each unit is copied into its buffer as soon as the tile's last S product of
+    // the previous unit has completed: one TMA box per 64 dims (128/G positions x the G heads
+    // of the group) when every row of the box lies inside q, else (the batch's last rows)
+    // plain 16-byte copies of the sequence's rows with zeros past it.
+    const int64_t q_rows = min((int64_t)__ldg(a.cu_seqlens_q + a.num_seqs), q_map_rows(a));
+    if (lane == 0) umma::prefetch_tmap(&tm_q);
+    uint32_t qep = 0, started = 0;  // per tile: parity of its next q_empty phase; first done
+    auto box_ok = [&](const UnitRec& u, int g) {
+      return (int64_t)u.q0 + u.i0 + g * P + P <= q_rows;
+    };
+    for (int k = 0; k < n_units; ++k) {
+      const UnitRec& u = recs[k];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        if (nt_of(u.nt, g) == 0) continue;
+        if ((started >> g) & 1u) {
+          if (lane == 0 && !mbar_wait(&ctl.q_empty[g], (qep >> g) & 1u, abort_flag))
+            note_timeout(ctl, a.dev_err);
+          qep ^= 1u << g;
+        }
+        started |= 1u << g;
+        __syncwarp();
+        unsigned char* qbuf = sm.q[g];
+        const int i0 = u.i0 + g * P;  // the tile's first position in the sequence
+        if (box_ok(u, g)) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&ctl.q_full[g], (uint32_t)(kRows * D * 2));
+#pragma unroll
+            for (int h2 = 0; h2 < NH; ++h2)
+              umma::tma_load_3d(qbuf + h2 * kHalf, &tm_q, h2 * 64, u.j * G, u.q0 + i0,
+                                &ctl.q_full[g]);
+          }
+        } else {
+          for (int r = lane; r < kRows; r += 32) {
+            const int qi = i0 + r / G;
+            const bool ok = qi < u.n;
+            const uint16_t* src = static_cast<const uint16_t*>(a.q) +
+                                  (ok ? ((int64_t)(u.q0 + qi) * H + u.j * G + r % G) * D : 0);
+#pragma unroll
+            for (int ch = 0; ch < D / 8; ++ch)
+              cp_async16_zfill(qbuf + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                               src + (ok ? ch * 8 : 0), ok ? 16u : 0u);
+          }
+          cp_async_wait_all();
+          fence_proxy_async_smem();  // written through the generic proxy, read by the MMA
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.q_full[g]);
+        }
+      }
+      // warm L2 with the next unit's Q (its copy waits for this unit's last S products)
+      if (lane == 0 && k + 1 < n_units) {
+        const UnitRec& x = recs[k + 1];
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+          if (nt_of(x.nt, g) > 0 && box_ok(x, g))
+            for (int h2 = 0; h2 < NH; ++h2)
+              umma::tma_prefetch_3d(&tm_q, h2 * 64, x.j * G, x.q0 + x.i0 + g * P);
       }
     }
   }
@@ -651,7 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;      // warp within the warpgroup (TMEM lane quarter)
     const int pos = r / G, hh = r % G;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    unsigned char* qbuf = sm.q[g];
     int sc = 0, oc = 0;  // s_full and o_done phases consumed
 
     // the first unit after k (k = -1: the first unit) in which this tile has rows
@@ -660,30 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nt_of(recs[k].nt, g) > 0) break;
       return k;
     };
-    // this row's Q of unit k into the tile's buffer (128-byte swizzled, K-major; rows past
-    // the sequence are zeros)
-    auto load_q = [&](int k) {
-      const UnitRec& x = recs[k];
-      const int qi = x.i0 + g * P + pos;
-      const bool ok = qi < x.n;
-      const uint16_t* src = static_cast<const uint16_t*>(a.q) +
-                            (ok ? ((int64_t)(x.q0 + qi) * H + x.j * G + hh) * D : 0);
-#pragma unroll
-      for (int ch = 0; ch < D / 8; ++ch)
-        cp_async16_zfill(qbuf + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
-                         src + (ok ? ch * 8 : 0), ok ? 16u : 0u);
-    };
-    auto q_landed = [&]() {
-      cp_async_wait_all();
-      fence_proxy_async_smem();  // written through the generic proxy, read by the MMA
-      mbar_arrive(&ctl.q_full[g]);
-    };
-
     int k = next_unit(-1);
-    if (k < n_units) {
-      load_q(k);
-      q_landed();
-    }
     while (k < n_units) {
       const int kn = next_unit(k);
       int lim_row, kv_len, vbase, my_nt;
@@ -695,26 +770,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         vbase = u.vbase;
         my_nt = nt_of(u.nt, g);
       }
-      // a few tiles before this unit's end: warm L2 with this row of the next unit's Q
-      // (copied in by cp.async at the last tile, when the Q buffer is free)
-      const int it_warm = kn < n_units ? max(0, my_nt - 3) : -1;
       float m_run = -INFINITY, l_run = 0.f;
       for (int it = 0; it < my_nt; ++it) {
         if (!mbar_wait(&ctl.s_full[g], (uint32_t)(sc & 1), abort_flag)) note_timeout(ctl, a.dev_err);
         ++sc;
         umma::fence_after_sync();
-        if (it == it_warm) {
-          const UnitRec& x = recs[kn];
-          const int qi = x.i0 + g * P + pos;
-          if (qi < x.n) {
-            const char* src = reinterpret_cast<const char*>(
-                static_cast<const uint16_t*>(a.q) + ((int64_t)(x.q0 + qi) * H + x.j * G + hh) * D);
-#pragma unroll
-            for (int b = 0; b < D * 2; b += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + b));
-          }
-        }
-        // the unit's last S product of this tile has completed: its Q buffer is free
-        if (it == my_nt - 1 && kn < n_units) load_q(kn);
         float sv[kKeys];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) umma::tmem_ld32(lane_addr + col_s(g) + 32 * c4, sv + 32 * c4);
@@ -799,8 +859,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::fence_before_sync();
         mbar_arrive(&ctl.p_full[g]);
       }
-      // the next unit's Q rows are in: its first S product may start
-      if (kn < n_units) q_landed();
 
       // ---- epilogue: O / l -> 16-bit rows --------------------------------------------
       if (!mbar_wait(&ctl.o_done[g], (uint32_t)(oc & 1), abort_flag)) note_timeout(ctl, a.dev_err);
@@ -816,7 +874,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) umma::tmem_ld32(lane_addr + col_o(g) + 32 * c4, ob + 32 * c4);
       umma::tmem_ld_wait();
-      if (row_ok) {
+      if (row_ok && (reinterpret_cast<uintptr_t>(a.out) & 31) == 0) {
+        // 32 bytes per store: one full sector each
+#pragma unroll
+        for (int q16 = 0; q16 < D / 16; ++q16) {
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = pack_elt2<F16>(ob[16 * q16 + 2 * e] * inv, ob[16 * q16 + 2 * e + 1] * inv);
+          asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 2 * q16),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                       "r"(w[6]), "r"(w[7])
+                       : "memory");
+        }
+      } else if (row_ok) {
 #pragma unroll
         for (int q8 = 0; q8 < D / 8; ++q8) {
           uint4 pk;
@@ -857,17 +928,19 @@ int launch_prefill_t(const PrefillArgs& a, const DeviceInfo& info, cudaStream_t 
   const int64_t max_pairs = qt_n * a.num_seqs;
   const int64_t max_units = max_pairs * a.num_kv_heads;
   PrefillArgs args = a;
+  CUtensorMap mq;
+  if (!make_rows_map(&mq, a.q, q_map_rows(a), a.num_heads, D, F16, G, P)) return PA_ERR_CUDA;
   // persistent (one CTA per SM, fewer when the batch has fewer units) when the in-kernel
   // sort and every CTA's records are sure to hold the batch; else one unit per CTA
   const int grid1 = (int)(max_units < info.num_sms ? max_units : info.num_sms);
   args.persistent = a.num_seqs <= kMaxSortSeqs && max_pairs <= kMaxSortPairs && grid1 > 0 &&
                     (max_units + grid1 - 1) / grid1 + 1 <= kMaxUnitRecs;
   if (args.persistent) {
-    paged_prefill_kernel<G, D, F16><<<grid1, kThreads, smem, stream>>>(mk, mv, args);
+    paged_prefill_kernel<G, D, F16><<<grid1, kThreads, smem, stream>>>(mk, mv, mq, args);
   } else {
     if (qt_n > 65535) return PA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)a.num_kv_heads, (unsigned)a.num_seqs, (unsigned)qt_n);
-    paged_prefill_kernel<G, D, F16><<<grid, kThreads, smem, stream>>>(mk, mv, args);
+    paged_prefill_kernel<G, D, F16><<<grid, kThreads, smem, stream>>>(mk, mv, mq, args);
   }
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
