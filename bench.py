@@ -71,7 +71,8 @@ def source_sha256(*names) -> str:
 
 DECODE_SOURCES = ("decode_kernel.cuh", "pa_device.cuh")
 DECODE_TC_SOURCES = ("decode_tc.cuh", "decode_kernel.cuh", "pa_device.cuh")
-PREFILL_SOURCES = ("prefill_kernel.cuh", "prefill.cu", "umma.cuh", "pa_device.cuh")
+PREFILL_SOURCES = ("prefill_kernel.cuh", "prefill.cu", "umma.cuh", "pa_device.cuh", "tensor_map.cu",
+                   "tensor_map.h")
 STORE_SOURCES = ("store.cu", "pa_device.cuh")
 
 
