@@ -724,15 +724,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&ctl.q_full[g]);
         }
       }
-      // warm L2 with the next unit's Q (its copy waits for this unit's last S products)
-      if (lane == 0 && k + 1 < n_units) {
-        const UnitRec& x = recs[k + 1];
-#pragma unroll
-        for (int g = 0; g < 2; ++g)
-          if (nt_of(x.nt, g) > 0 && box_ok(x, g))
-            for (int h2 = 0; h2 < NH; ++h2)
-              umma::tma_prefetch_3d(&tm_q, h2 * 64, x.j * G, x.q0 + x.i0 + g * P);
-      }
     }
   }
     // ---- teardown: every role is done with tensor memory
