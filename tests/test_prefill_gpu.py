@@ -76,6 +76,33 @@ def test_single_token_prefill_equals_decode():
     np.testing.assert_allclose(to_f64(out), to_f64(dec), atol=2e-2, rtol=2e-2)
 
 
+def test_q_rows_after_an_offset():
+    """cu_seqlens_q starting past row 0: the first rows of q and out belong to no sequence.
+    The later tiles lie past the host's bound on the batch's rows (num_seqs x max_seqlen_q),
+    so their Q rows are copied row by row while the earlier ones come by whole TMA boxes;
+    rows outside the sequences are never written."""
+    import dataclasses
+    base = workloads.prefill_case([0, 130, 700], [200, 77, 129], 16, 8, 128, 256, seed=1250)
+    off = 300
+    rng = np.random.default_rng(1251)
+    lead = torch.from_numpy(rng.standard_normal((off,) + tuple(base.q.shape[1:])).astype(
+        np.float32)).to(base.q.dtype)
+    case = dataclasses.replace(base, q=torch.cat([lead, base.q]),
+                               cu_seqlens_q=(base.cu_seqlens_q + off).astype(np.int32))
+    dc = DeviceCase(case)
+    dc.store()
+    out = dc.prefill()
+    assert dc.dev_err() == 0, f"device error bits {dc.dev_err()}"
+    # the oracle takes rows from 0: the same sequences without the leading rows
+    ok, ov = oracle_after_store(base)
+    ref = oracle.prefill(base.q, from_bits(ok), from_bits(ov), base.block_tables,
+                         base.cu_seqlens_q, base.cu_seqlens_k, causal=True)
+    got = to_f64(out)
+    assert np.all(np.isnan(got[:off])), "rows before the first sequence were written"
+    assert np.all(np.isfinite(got[off:]))
+    assert_close(got[off:], ref, "q rows after an offset")
+
+
 def test_prefill_deterministic():
     case = workloads.prefill_case([100, 0], [300, 257], 16, 8, 128, 256, seed=1300)
     dc = DeviceCase(case)
