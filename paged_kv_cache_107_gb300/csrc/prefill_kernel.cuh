@@ -51,8 +51,8 @@
 //    Rows of the last V tile past the sequence are zeroed, so stale or poisoned rows never
 //    meet a zero probability.
 //  * Every wait is bounded; on a timeout the kernel records PA_DEV_ERR_TIMEOUT, runs to
-//    the end of its protocol (the producer still waits for its own copies) and frees its
-//    tensor memory.
+//    the end of its protocol (the K/V and Q warps still wait for their own copies) and
+//    frees its tensor memory.
 #pragma once
 
 #include <atomic>
@@ -682,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t q_rows = min((int64_t)__ldg(a.cu_seqlens_q + a.num_seqs), q_map_rows(a));
     if (lane == 0) umma::prefetch_tmap(&tm_q);
     uint32_t qep = 0, started = 0;  // per tile: parity of its next q_empty phase; first done
+    int qn[2] = {0, 0};             // Q copies issued per tile (one q_full phase each)
     auto box_ok = [&](const UnitRec& u, int g) {
       return (int64_t)u.q0 + u.i0 + g * P + P <= q_rows;
     };
@@ -696,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           qep ^= 1u << g;
         }
         started |= 1u << g;
+        ++qn[g];
         __syncwarp();
         unsigned char* qbuf = sm.q[g];
         const int i0 = u.i0 + g * P;  // the tile's first position in the sequence
@@ -724,6 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&ctl.q_full[g]);
         }
       }
+    }
+    // each tile's last copy lands before the CTA may exit (the full limit even after a
+    // timeout elsewhere: a copy must not outlive the CTA's shared memory)
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (qn[g] > 0) mbar_wait_copies(&ctl.q_full[g], (uint32_t)((qn[g] - 1) & 1));
     }
   }
     // ---- teardown: every role is done with tensor memory
