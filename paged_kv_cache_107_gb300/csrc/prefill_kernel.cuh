@@ -90,9 +90,13 @@ constexpr int kMaxSortSeqs = 1024;
 constexpr int kMaxSortPairs = 2048;
 constexpr int kRankSortMax = 512;  // up to this many entries a rank sort, else bitonic
 
-// TMEM columns: S (then P) of tile g at g*128, O of tile g at 256 + g*128.
+// TMEM columns: S (then P) of tile g at g*128, O of tile g at 256 + g*128. At head_dim 64,
+// O takes the first 64 of its 128 columns and P gets the other 64 (320 + g*128), so that
+// the next S product may be issued as soon as the softmax has read this one (not after
+// this tile's P.V).
 __host__ __device__ constexpr uint32_t col_s(int g) { return (uint32_t)(g * 128); }
 __host__ __device__ constexpr uint32_t col_o(int g) { return (uint32_t)(256 + g * 128); }
+__host__ __device__ constexpr uint32_t col_p(int g) { return (uint32_t)(320 + g * 128); }
 
 // One work unit of a CTA, as a record in shared memory.
 struct UnitRec {
@@ -116,7 +120,9 @@ struct PrefillCtl {
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];  // PV products of that V stage done
   uint64_t s_full[2];          // [tile]
+  uint64_t s_free[2];          // [tile] head_dim 64: the softmax has read its S
   uint64_t p_full[2];
+  uint64_t pv_done[2];         // [tile] head_dim 64: a P.V product done (one phase each)
   uint64_t o_done[2];          // the tile's last PV of a unit done
   uint32_t tmem_base;
   int abort;
@@ -421,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tm_q, const PrefillArgs a) {
   constexpr int P = kRows / G;  // query positions per tile
   constexpr int NH = D / 64;    // 64-dim swizzled column blocks per row
+  constexpr bool kSepP = D == 64;  // P in its own tensor-memory columns (see col_p)
   using Tiles = PrefillTiles<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   PrefillCtl& ctl = *reinterpret_cast<PrefillCtl*>(smem_raw);
@@ -456,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&ctl.s_full[g], 1);
+      mbar_init(&ctl.s_free[g], kRows);
       mbar_init(&ctl.p_full[g], kRows);
+      mbar_init(&ctl.pv_done[g], 1);
       mbar_init(&ctl.o_done[g], 1);
     }
     ctl.abort = 0;
@@ -578,11 +587,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kc = 0, vc = 0;      // K and V loads consumed
       int qc[2] = {0, 0};      // Q tiles consumed, per tile slot
       int pc[2] = {0, 0};      // P tiles consumed, per tile slot
+      int s_cnt[2] = {0, 0};   // S products issued, per tile slot
       auto commit1 = [&](uint64_t* bar) {  // arrival on bar once the products so far are done
         if (elect_one()) umma::commit(bar);
         __syncwarp();
       };
       auto issue_s = [&](int g, int kstage) {  // S_g = Q_g K^T
+        if constexpr (kSepP) {
+          // S_g is overwritten once the softmax has read the previous one
+          if (s_cnt[g] > 0 &&
+              !mbar_wait(&ctl.s_free[g], (uint32_t)((s_cnt[g] - 1) & 1), abort_flag))
+            note_timeout(ctl, a.dev_err);
+          umma::fence_after_sync();
+          ++s_cnt[g];
+        }
         // descriptors of the K-slice kk: the tile's base descriptor plus the slice's offset
         // in 16-byte units (the address field cannot carry: shared addresses are < 256 KB)
         const uint64_t qd = umma::smem_desc(smem_u32(sm.q[g]), 16, 1024);
@@ -602,8 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
-            umma::mma_bf16_ts(tmem + col_o(g), tmem + col_s(g) + kk * 8,
+            umma::mma_bf16_ts(tmem + col_o(g), tmem + (kSepP ? col_p(g) : col_s(g)) + kk * 8,
                               vd + ((kk * 16 * 128) >> 4), idesc_o, !first || (kk > 0));
+          if constexpr (kSepP) umma::commit(&ctl.pv_done[g]);
         }
         __syncwarp();
       };
@@ -636,6 +655,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = recs[k].nt;
         const int n_all = nt_all(nt);
         for (int it = 0; it < n_all; ++it) {
+          if constexpr (kSepP) {
+            // S(it+1) of each tile first (each waits only for its softmax to have read
+            // S(it)), then PV(it) of each tile once its P is written
+            if (it + 1 < n_all) {
+              wait_k();
+#pragma unroll
+              for (int g = 0; g < 2; ++g) {
+                const int ntg = nt_of(nt, g);
+                if (it + 1 >= ntg) continue;
+                issue_s(g, kc % kKStages);
+                if (it + 2 == ntg) commit1(&ctl.q_empty[g]);  // the unit's last S_g
+              }
+              commit1(&ctl.k_empty[kc % kKStages]);
+              ++kc;
+            }
+            bool vr = false;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const int ntg = nt_of(nt, g);
+              if (it >= ntg) continue;
+              if (!mbar_wait(&ctl.p_full[g], (uint32_t)(pc[g] & 1), abort_flag))
+                note_timeout(ctl, a.dev_err);
+              ++pc[g];
+              if (!vr) {
+                if (!mbar_wait(&ctl.v_full[vc % kVStages], (uint32_t)((vc / kVStages) & 1),
+                               abort_flag))
+                  note_timeout(ctl, a.dev_err);
+                vr = true;
+              }
+              umma::fence_after_sync();
+              issue_pv(g, vc % kVStages, it == 0);
+              if (it == ntg - 1) commit1(&ctl.o_done[g]);
+            }
+            commit1(&ctl.v_empty[vc % kVStages]);
+            ++vc;
+            continue;
+          }
           bool v_ready = false, k_ready = false;
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
@@ -750,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;      // warp within the warpgroup (TMEM lane quarter)
     const int pos = r / G, hh = r % G;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    int sc = 0, oc = 0;  // s_full and o_done phases consumed
+    int sc = 0, oc = 0;  // s_full and o_done phases consumed (sc: S tiles of this query tile)
 
     // the first unit after k (k = -1: the first unit) in which this tile has rows
     auto next_unit = [&](int k) {
@@ -779,6 +835,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) umma::tmem_ld32(lane_addr + col_s(g) + 32 * c4, sv + 32 * c4);
         umma::tmem_ld_wait();
+        if constexpr (kSepP) {  // S_g may be overwritten by the next product
+          umma::fence_before_sync();
+          mbar_arrive(&ctl.s_free[g]);
+        }
 
         const int t0 = it * kKeys;
         // only tiles that reach past this row's last visible key need a mask
@@ -826,9 +886,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 tt = umma::fadd2(t01, t23);
         l_run = l_run * alpha + (tt.x + tt.y);
         m_run = m_use;
-        umma::tmem_st32(lane_addr + col_s(g), sv);
-        umma::tmem_st32(lane_addr + col_s(g) + 32, sv + 32);
-        // O_g is stable here (S_g(it) completed after PV_g(it-1)); PV_g(it) waits for p_full
+        if constexpr (kSepP) {
+          // the previous P.V of this tile has read P_g and landed in O_g (its pv_done phase;
+          // the one before completed before this S product was issued)
+          if (sc > 1 &&
+              !mbar_wait(&ctl.pv_done[g], (uint32_t)((sc - 2) & 1), abort_flag))
+            note_timeout(ctl, a.dev_err);
+          umma::fence_after_sync();
+          umma::tmem_st32(lane_addr + col_p(g), sv);
+          umma::tmem_st32(lane_addr + col_p(g) + 32, sv + 32);
+        } else {
+          umma::tmem_st32(lane_addr + col_s(g), sv);
+          umma::tmem_st32(lane_addr + col_s(g) + 32, sv + 32);
+        }
+        // O_g is stable here (head_dim 128: S_g(it) completed after PV_g(it-1); 64: waited
+        // above); PV_g(it) waits for p_full
         if (__any_sync(0xffffffffu, rescale)) {
           float ob[32];
 #pragma unroll
