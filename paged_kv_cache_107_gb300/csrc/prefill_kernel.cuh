@@ -42,8 +42,10 @@
 //    straight from tensor memory (B = V, MN-major) into 128 more columns per tile. On the
 //    tensor core the order per key tile is PV_A(i), S_A(i+1), PV_B(i), S_B(i+1): each S is
 //    issued only after the PV that reads the P it overwrites, and S_g(i) completes after
-//    PV_g(i-1), so O_g is stable whenever the softmax sees a new S_g. Key tiles past the
-//    causal limit of tile A are not multiplied for A.
+//    PV_g(i-1), so O_g is stable whenever the softmax sees a new S_g. At head_dim 64 P has
+//    columns of its own: S_A(i+1), S_B(i+1) follow the softmax's read of S(i) and come
+//    before PV_A(i), PV_B(i); the softmax touches P and O only after the previous PV has
+//    landed. Key tiles past the causal limit of tile A are not multiplied for A.
 //  * Softmax: 8 warps, thread r of a warpgroup owns row r of its tile (TMEM lane r): scores
 //    are masked by key index (causal and length) on boundary tiles only, reduced with tree
 //    max/sum, the running max is only moved when it grows by more than 2^8 (then O is
