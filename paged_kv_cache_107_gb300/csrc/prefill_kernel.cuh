@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the stream of key tiles (units in order, tiles in order): lane b
     // reads box b's block id, two tiles ahead of the K load that first needs it (the V load
     // of the same tile reuses it), so the table's latency stays off the copies' path; lane
-    // 0 waits for free stages and issues the copies.
+    // 0 waits for free stages, and each box's lane issues its copy.
     if (lane == 0) {
       umma::prefetch_tmap(&tm_k);
       umma::prefetch_tmap(&tm_v);
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kc = 0, vc = 0;      // K and V loads consumed
       int qc[2] = {0, 0};      // Q tiles consumed, per tile slot
       int pc[2] = {0, 0};      // P tiles consumed, per tile slot
-      int s_cnt[2] = {0, 0};   // S products issued, per tile slot
+      int s_cnt[2] = {0, 0};   // head_dim 64: S products issued, per tile slot
       auto commit1 = [&](uint64_t* bar) {  // arrival on bar once the products so far are done
         if (elect_one()) umma::commit(bar);
         __syncwarp();
