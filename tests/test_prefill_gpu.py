@@ -21,14 +21,15 @@ def run_prefill(case, rows=None):
     out = dc.prefill()
     assert dc.dev_err() == 0, f"device error bits {dc.dev_err()}"
     ok, ov = oracle_after_store(case)
+    dt = case.k_cache.dtype
     got = to_f64(out)
     if rows is None:
-        ref = oracle.prefill(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+        ref = oracle.prefill(case.q, from_bits(ok, dt), from_bits(ov, dt), case.block_tables,
                              case.cu_seqlens_q, case.cu_seqlens_k, causal=case.causal)
         assert np.all(np.isfinite(got))
         assert_close(got, ref, case.name)
     else:
-        ref = oracle.prefill(case.q, from_bits(ok), from_bits(ov), case.block_tables,
+        ref = oracle.prefill(case.q, from_bits(ok, dt), from_bits(ov, dt), case.block_tables,
                              case.cu_seqlens_q, case.cu_seqlens_k, causal=case.causal, rows=rows)
         flat = got.reshape(-1, case.head_dim)[rows]
         assert np.all(np.isfinite(flat))
@@ -147,6 +148,16 @@ def test_schedule_one_unit_per_cta_beyond_sort_limit():
     cached = rng.integers(0, 41, 1100)
     new = rng.integers(1, 4, 1100)
     run_prefill(workloads.prefill_case(cached, new, 16, 8, 128, 16, seed=1401))
+
+
+def test_schedule_one_unit_per_cta_head_dim_64_fp16():
+    """The same grid at head_dim 64 with IEEE fp16 elements (P in its own tensor-memory
+    columns, the next S product issued once the softmax has read the last): every row."""
+    rng = np.random.default_rng(1410)
+    cached = rng.integers(0, 41, 1100)
+    new = rng.integers(1, 4, 1100)
+    run_prefill(workloads.prefill_case(cached, new, 16, 8, 64, 16, seed=1411,
+                                       dtype=torch.float16))
 
 
 def test_schedule_persistent_with_many_units_per_cta():
