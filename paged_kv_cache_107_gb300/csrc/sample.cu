@@ -16,7 +16,7 @@
 // Design (the logits are read once; the arithmetic is one Philox block per 4 elements and
 // two or three special-function operations per element):
 //  * Rows that start on 16 bytes: a persistent CTA per SM takes an even share of the
-//    (row, 32 KB tile) stream. A producer warp moves tiles with cp.async.bulk into a
+//    (row, tile of 40 KB for fp32, 24 KB for bf16) stream. A producer warp moves tiles with cp.async.bulk into a
 //    4-stage shared-memory ring (mbarrier full/empty pairs, bounded waits); consumer
 //    warps score them from shared memory, one 16-byte group per thread at a time.
 //  * Other rows: one CTA per (row, 8192-element chunk) with plain loads.
@@ -39,10 +39,10 @@ namespace {
 
 constexpr int kSampleThreads = 256;
 constexpr int kSampleChunk = 8192;  // elements per CTA of the plain-load kernel
-#ifndef PA_SAMPLE_RING_WARPS
-#define PA_SAMPLE_RING_WARPS 16
-#endif
-constexpr int kSampleRingWarps = PA_SAMPLE_RING_WARPS;  // consumer warps of the ring kernel
+// consumer warps of the ring kernel (measured on B=256, V=151936: fp32 59.6-60.4 us at 20
+// against 61.3-61.9 at 16 and 61.4 at 24; bf16 58.8-59.2 us at 12 against 61.4-63.4 at 16,
+// where 20 warps leave too few registers and spill)
+constexpr int kRingWarpsF32 = 20, kRingWarpsBf16 = 12;
 
 __device__ __forceinline__ void philox4x32_10(uint32_t& c0, uint32_t& c1, uint32_t& c2,
                                               uint32_t& c3, uint32_t k0, uint32_t k1) {
@@ -64,32 +64,31 @@ __device__ __forceinline__ void philox4x32_10(uint32_t& c0, uint32_t& c1, uint32
   }
 }
 
-// -log2(u) for u = (2k + 1) / 2^24, k the top 23 bits of `bits`, with relative accuracy
-// over the whole range. u = (1 + k/2^23) - (1 - 2^-24) and w = 1 - u =
-// (1 + (2^23 - 1 - k)/2^23) - (1 - 2^-24) are both exact in binary32. For u <= 0.9 the
-// hardware log2 (absolute error about 2^-22 on [1/2, 2], and |log2 u| >= 0.15, so at most
-// about 2e-6 relative); for u > 0.9, -log2(1 - w) = (2 / ln 2) atanh(s) with
-// s = w / (2 - w) < 0.053, summed by the Taylor series of atanh up to s^5 (truncation below
-// 1e-8 relative).
-__device__ __forceinline__ float neg_log2_uniform(uint32_t bits) {
-  const uint32_t k = bits >> 9;
-  const float u = __uint_as_float(0x3F800000u | k) - 0.99999994039535522f;
-  const float w = __uint_as_float(0x3F800000u | (k ^ 0x7FFFFFu)) - 0.99999994039535522f;
-  const float a = -fast_log2(u);
+// log2(u) (negative) for u = (2k + 1) / 2^24, k the top 23 bits of `bits`, with relative
+// accuracy over the whole range. u = (1 + k/2^23) - (1 - 2^-24) is exact in binary32, and
+// so is w = 1 - u (Sterbenz: u >= 1/2 where it is used). For u <= 0.9 the hardware log2
+// (absolute error about 2^-22 on [1/2, 2], and |log2 u| >= 0.15, so at most about 2e-6
+// relative); for u > 0.9, log2(1 - w) = -(2 / ln 2) atanh(s) with s = w / (1 + u) < 0.053
+// (1 + u = 2 - w), summed by the Taylor series of atanh up to s^5 (truncation below 1e-8
+// relative), the sign carried by the coefficients.
+__device__ __forceinline__ float log2_uniform(uint32_t bits) {
+  const float u = __uint_as_float(0x3F800000u + (bits >> 9)) - 0.99999994039535522f;
+  const float w = 1.f - u;
+  const float a = fast_log2(u);
   float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(2.f - w));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + u));
   const float s = w * r;
   const float s2 = s * s;
-  float p = 0.57707801635558540f;         // (2 / ln 2) / 5
-  p = fmaf(p, s2, 0.96179669392597560f);  // (2 / ln 2) / 3
-  p = fmaf(p, s2, 2.88539008177792680f);  // 2 / ln 2
-  // u <= 0.9 exactly when k <= 7549746 (u = (2k + 1) / 2^24)
-  return k <= 7549746u ? a : s * p;
+  float p = -0.57707801635558540f;         // -(2 / ln 2) / 5
+  p = fmaf(p, s2, -0.96179669392597560f);  // -(2 / ln 2) / 3
+  p = fmaf(p, s2, -2.88539008177792680f);  // -2 / ln 2
+  // u <= 0.9 exactly when k <= 7549746 (u = (2k + 1) / 2^24), i.e. bits < 7549747 * 2^9
+  return bits < 3865470464u ? a : s * p;
 }
 
 // Ranking score of one element in log2 units: l * (log2(e) / T) - log2(-log2 u).
 __device__ __forceinline__ float rank_score(float l, float scale, uint32_t bits) {
-  return fmaf(l, scale, -fast_log2(neg_log2_uniform(bits)));
+  return fmaf(l, scale, -fast_log2(-log2_uniform(bits)));
 }
 
 __device__ __forceinline__ uint64_t score_key(float x, int64_t i) {
@@ -203,13 +202,64 @@ __global__ void __launch_bounds__(kSampleThreads) gumbel_sample_chunk_kernel(con
 }
 
 // ---------------------------------------------------------------- ring kernel
+// Maximum of the NE (a power of two) scores of a thread's tile by a pairwise tree: node v
+// (1 <= v < NE) holds the maximum of its children 2v and 2v + 1, nodes NE..2NE-1 are the
+// leaves xs[0..NE-1]. fmaxf skips NaN, so a node is NaN only if all leaves under it are.
+template <int NE>
+__device__ __forceinline__ float tree_node(const float (&xs)[NE], const float (&t)[NE], int v) {
+  return v >= NE ? xs[v - NE] : t[v];
+}
+
+template <int NE>
+__device__ __forceinline__ float tree_max(const float (&xs)[NE], float (&t)[NE]) {
+#pragma unroll
+  for (int v = NE - 1; v >= 1; --v) t[v] = fmaxf(tree_node(xs, t, 2 * v), tree_node(xs, t, 2 * v + 1));
+  return t[1];
+}
+
+// The first leaf holding the (non-NaN) maximum t[1]: from the root down, the left child
+// when it equals the maximum (then a leaf under it does), else the right one. The left
+// child of the node reached so far is picked out of its level by selects on the decisions
+// already taken, so no array is indexed at run time.
+template <int NE>
+__device__ __forceinline__ int first_index_of_max(const float (&xs)[NE], const float (&t)[NE]) {
+  constexpr int kLevels = __builtin_ctz(NE);
+  static_assert((1 << kLevels) == NE, "power of two");
+  const float m = t[1];
+  bool right[kLevels];
+#pragma unroll
+  for (int lev = 0; lev < kLevels; ++lev) {
+    // left children of the 2^lev nodes of this level, in order (constant trip counts, so
+    // that every loop unrolls and c stays in registers)
+    float c[NE / 2];
+#pragma unroll
+    for (int i = 0; i < NE / 2; ++i)
+      if (i < (1 << lev)) c[i] = tree_node(xs, t, 2 * ((1 << lev) + i));
+#pragma unroll
+    for (int b = 0; b < kLevels; ++b)  // fold by the latest decision first
+      if (b < lev) {
+#pragma unroll
+        for (int i = 0; i < NE / 4; ++i)
+          if (i < (1 << (lev - b - 1))) c[i] = right[lev - 1 - b] ? c[2 * i + 1] : c[2 * i];
+      }
+    right[lev] = !(c[0] == m);
+  }
+  int j = 0;
+#pragma unroll
+  for (int lev = 0; lev < kLevels; ++lev) j = 2 * j + (right[lev] ? 1 : 0);
+  return j;
+}
+
 constexpr int kRingStages = 4;
-constexpr int kTileBytes = 32768;
+// a tile is four 16-byte groups per consumer thread (40 KB with 20 consumer warps, 24 KB
+// with 12)
+template <int CW>
+constexpr int ring_tile_bytes() { return CW * 32 * 16 * 4; }
 
 struct RingCtrl {
   uint64_t full[kRingStages];
   uint64_t empty[kRingStages];
-  uint64_t slots[2][16];
+  uint64_t slots[2][32];  // one key per consumer warp
   int abort;
 };
 
@@ -218,6 +268,8 @@ struct RingCtrl {
 template <typename T, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(const SampleArgs a) {
   constexpr int EPG = 16 / sizeof(T);            // elements per 16-byte group
+  constexpr int kTileBytes = ring_tile_bytes<CW>();
+  static_assert(CW <= 32, "one key slot per consumer warp");
   constexpr int TE = kTileBytes / sizeof(T);     // elements per tile
   constexpr int CT = CW * 32;                    // consumer threads
   constexpr int GPT = kTileBytes / 16 / CT;      // groups per consumer thread per tile
@@ -248,10 +300,10 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(co
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t policy = policy_evict_first();
-      for (int64_t it = 0; it < n_tiles; ++it) {
-        const int64_t x = x0 + it;
-        const int b = (int)(x / a.chunks);
-        const int64_t start = (x - (int64_t)b * a.chunks) * TE;
+      int b = (int)(x0 / a.chunks), ci = (int)(x0 - (int64_t)b * a.chunks);  // row, tile in row
+      for (int64_t it = 0; it < n_tiles; ++it, ci = ci + 1 == a.chunks ? 0 : ci + 1,
+                   b += ci == 0 ? 1 : 0) {
+        const int64_t start = (int64_t)ci * TE;
         const int64_t n = min((int64_t)TE, (int64_t)a.vocab - start);
         const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(T)) & ~15u;
         const int st = (int)(it % kRingStages);
@@ -281,11 +333,17 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(co
   bool greedy = true;
   uint32_t k0 = 0, k1 = 0, o0 = 0, o1 = 0;
   uint32_t rk0[10], rk1[10];  // Philox round keys of the current row
+  // Counter words 1-3 of every block of a row are (0, offset lo, offset hi), so part of
+  // rounds 0 and 1 is the same for the whole row. Round 0 leaves c0 = h0, c1 = h1,
+  // c2 = hi(M0 ctr) ^ hb, c3 = lo(M0 ctr); round 1 then gives c0 = hi(M1 c2) ^ h2,
+  // c1 = lo(M1 c2), c2 = c3 ^ h3 and c3 = h4, where h0..h4 and hb depend on the row only.
+  uint32_t h0 = 0, h1 = 0, h2 = 0, h3 = 0, h4 = 0, hb = 0;
   auto sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory"); };
-  for (int64_t it = 0; it < n_tiles; ++it) {
-    const int64_t x = x0 + it;
-    const int b = (int)(x / a.chunks);
-    const int64_t start = (x - (int64_t)b * a.chunks) * TE;
+  // row and tile within the row of tile x0 + it, advanced without a division per tile
+  int b = (int)(x0 / a.chunks), ci = (int)(x0 - (int64_t)b * a.chunks);
+  for (int64_t it = 0; it < n_tiles; ++it, ci = ci + 1 == a.chunks ? 0 : ci + 1,
+               b += ci == 0 ? 1 : 0) {
+    const int64_t start = (int64_t)ci * TE;
     const int64_t n = min((int64_t)TE, (int64_t)a.vocab - start);
     const int64_t n_bulk = ((n * (int64_t)sizeof(T)) & ~int64_t(15)) / (int64_t)sizeof(T);
     if (b != cur) {
@@ -309,6 +367,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(co
       }
       o0 = (uint32_t)off;
       o1 = (uint32_t)(off >> 32);
+      {
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * o0;  // round 0: M1 * c2, c2 = offset lo
+        h0 = (uint32_t)(p1 >> 32) ^ rk0[0];              // c1 = 0
+        h1 = (uint32_t)p1;
+        hb = o1 ^ rk1[0];                                // round 0: c3 ^ k1
+        const uint64_t p0 = (uint64_t)0xD2511F53u * h0;  // round 1: M0 * c0
+        h2 = h1 ^ rk0[1];
+        h3 = (uint32_t)(p0 >> 32) ^ rk1[1];
+        h4 = (uint32_t)p0;
+      }
       best_x = -INFINITY;
       best_i = start + (int64_t)tid * EPG;  // all -inf / NaN: the row's first element
     }
@@ -361,13 +429,18 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(co
 #pragma unroll
       for (int q = 0; q < NB; ++q) {
         const int k = q / (EPG / 4), h = q % (EPG / 4);
-        c0[q] = (uint32_t)((s0 + (k * CT + tid) * EPG) >> 2) + h;
-        c1[q] = 0;
-        c2[q] = o0;
-        c3[q] = o1;
+        const uint32_t ctr = (uint32_t)((s0 + (k * CT + tid) * EPG) >> 2) + h;
+        uint64_t p0, p1;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(0xD2511F53u), "r"(ctr));  // round 0
+        const uint32_t x2 = (uint32_t)(p0 >> 32) ^ hb;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(0xCD9E8D57u), "r"(x2));   // round 1
+        c0[q] = (uint32_t)(p1 >> 32) ^ h2;
+        c1[q] = (uint32_t)p1;
+        c2[q] = (uint32_t)p0 ^ h3;
+        c3[q] = h4;
       }
 #pragma unroll
-      for (int r = 0; r < 10; ++r) {
+      for (int r = 2; r < 10; ++r) {
 #pragma unroll
         for (int q = 0; q < NB; ++q) {
           uint64_t p0, p1;
@@ -389,20 +462,18 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gumbel_sample_ring_kernel(co
         xs[4 * q + 3] = rank_score(xs[4 * q + 3], scale, c3[q]);
       }
     }
+    if (nb < TE) {  // only a row's last tile is short
 #pragma unroll
-    for (int k = 0; k < GPT; ++k)
-      if ((k * CT + tid) * EPG >= nb) {
+      for (int k = 0; k < GPT; ++k)
+        if ((k * CT + tid) * EPG >= nb) {
 #pragma unroll
-        for (int e = 0; e < EPG; ++e) xs[k * EPG + e] = -INFINITY;  // past the bulk part
-      }
-    float m = xs[0];
-#pragma unroll
-    for (int j = 1; j < NE; ++j) m = fmaxf(m, xs[j]);  // NaN is skipped by fmaxf
+          for (int e = 0; e < EPG; ++e) xs[k * EPG + e] = -INFINITY;  // past the bulk part
+        }
+    }
+    float t[NE];
+    const float m = tree_max(xs, t);
     if (m > best_x) {
-      int jj = 0;
-#pragma unroll
-      for (int j = NE - 1; j >= 0; --j)
-        if (xs[j] == m) jj = j;  // the first element holding the maximum
+      const int jj = first_index_of_max(xs, t);
       best_x = m;
       best_i = s0 + ((jj / EPG) * CT + tid) * EPG + (jj % EPG);
     }
@@ -438,7 +509,7 @@ size_t sample_workspace_bytes(int num_rows) {
 namespace {
 template <typename T, int CW>
 int launch_ring(const SampleArgs& a, cudaStream_t stream, int num_sms) {
-  const size_t smem = (size_t)kRingStages * kTileBytes + sizeof(RingCtrl) + 128;
+  const size_t smem = (size_t)kRingStages * ring_tile_bytes<CW>() + sizeof(RingCtrl) + 128;
   static std::atomic<bool> attr_done[64];  // zero-initialised: false
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
@@ -475,9 +546,10 @@ int launch_gumbel_sample(int64_t* out, const void* logits, int64_t row_stride, i
   const int esz = is_bf16 ? 2 : 4;
   const bool ring = (reinterpret_cast<uintptr_t>(logits) & 15) == 0 && ((row_stride * esz) & 15) == 0;
   if (ring) {
-    a.chunks = (int)(((int64_t)vocab * esz + kTileBytes - 1) / kTileBytes);
-    return is_bf16 ? launch_ring<uint16_t, kSampleRingWarps>(a, stream, num_sms)
-                   : launch_ring<float, kSampleRingWarps>(a, stream, num_sms);
+    const int tile = is_bf16 ? ring_tile_bytes<kRingWarpsBf16>() : ring_tile_bytes<kRingWarpsF32>();
+    a.chunks = (int)(((int64_t)vocab * esz + tile - 1) / tile);
+    return is_bf16 ? launch_ring<uint16_t, kRingWarpsBf16>(a, stream, num_sms)
+                   : launch_ring<float, kRingWarpsF32>(a, stream, num_sms);
   }
   a.chunks = (vocab + kSampleChunk - 1) / kSampleChunk;
   const int64_t grid = (int64_t)a.chunks * num_rows;

@@ -84,10 +84,12 @@ def test_qwen3_vocab_bf16():
     assert check(got, logits, temps, seeds, offs) > 0.99
 
 
-@pytest.mark.parametrize("V", [1, 3, 4, 5, 7, 8, 9, 4095, 8191, 8192, 8193, 16384, 20001])
+@pytest.mark.parametrize("V", [1, 3, 4, 5, 7, 8, 9, 4095, 8191, 8192, 8193, 10239, 10240,
+                               10241, 12287, 12288, 12289, 16384, 20001, 20480, 24577])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_vocab_edges(V, dtype):
-    """Single element, ragged 16-byte groups, chunk boundaries (8192 elements)."""
+    """Single element, ragged 16-byte groups, the ring's tile boundaries (10240 fp32 or
+    12288 bf16 elements) and the plain-load kernel's chunk boundaries (8192 elements)."""
     logits, temps, seeds, offs = inputs(12, V, 107310 + V, dtype=dtype, greedy_every=4)
     got = run(logits, temps, seeds, offs)
     assert (got >= 0).all() and (got < V).all()
