@@ -2,7 +2,7 @@
 "Model Runner V2 设计文档", section 6 "Gumbel 采样内核").
 
 The kernel decides in fp32 (logit * log2(e)/T + noise, the noise from the hardware log2
-and, for u > 0.9, an atanh series on the exact 1 - u), the oracle in fp64 from the same
+and, for u > 0.9, a fitted cubic in the exact 1 - u), the oracle in fp64 from the same
 32-bit random words. So a row must give
 exactly the oracle's index whenever the oracle's best score leads the runner-up by more
 than the fp32 error bound TOL; inside that bound (a near-tie, where both indices are
