@@ -572,7 +572,10 @@ def measure_variants(dev, steps: int, warmup: int, only=None, pool_blocks=None):
             "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak,
             "alg_bytes_per_launch": alg,
             "loop_step_us": loop_ms * 1e3,
-            "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9}
+            "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9,
+            # back to back, as the headline step loop runs: the same bytes over the loop's
+            # time per step (each launch a dependent of the one before)
+            "loop_frac_of_hbm": alg / (loop_ms * 1e-3) / 1e9 / hbm_peak}
         summary = {"g8": "decode_tc_g8_w2_b256.md", "d64_bf16": "decode_tc_d64_w2_b256.md"}
         if tag in summary:
             res["decode_step_" + tag]["traffic"] = kernel_traffic(
@@ -640,6 +643,7 @@ def measure_long_context(dev, steps: int, warmup: int, pool_blocks=None):
         "kv_bytes_per_step": kv_bytes, "step_us": ms * 1e3,
         "kv_gbs": kv_bytes / (ms * 1e-3) / 1e9, "seqs_per_s": case.num_seqs / (ms * 1e-3),
         "loop_step_us": loop_ms * 1e3, "loop_kv_gbs": kv_bytes / (loop_ms * 1e-3) / 1e9,
+        "loop_frac_of_hbm": alg / (loop_ms * 1e-3) / 1e9 / hbm_peak,
         "pct_of_nominal_hbm": 100.0 * kv_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
         "roofline": {"kernel": kname, "bound": "hbm", "unit": "GB/s",
                      "achieved": alg / (ms * 1e-3) / 1e9, "peak": hbm_peak,
